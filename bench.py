@@ -1,0 +1,446 @@
+"""Benchmark of one decode step: KV append, self-attention, cross-attention of
+every layer, then the fused sampler, on one batch of synthetic input.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl ours|reference]
+
+Default workload: 5, the batch-128 stress case (24 layers, paged bf16 KV with
+block size 16, self lengths U{512..4096}, cross 256, sampler 128x9x1088 with
+planted ties, top-k 250, T=0.7, per-row seeds) -- the batch >= 32 regime in
+which the self-attention's HBM bandwidth is the figure of merit.  Workloads
+1-4 are available with --workload.
+
+Metric: algorithmic HBM GB/s of the whole decode step (bytes the step must
+move: valid K/V, q, outputs, block-table entries, appended rows, logits and
+tokens) divided by the step time, summed over ranks (each rank a replica with
+its own batch: weak scaling, no collective on the data path).  The line also
+carries the step time, the self-attention kernel's roofline, the sampler time,
+an end-to-end figure with host buffers, and the CPU oracle timed on a bounded
+sample (cpu_baseline).  --impl reference times that oracle alone.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import dataclasses
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from decode_attention_self_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode-step attention µs & HBM GB/s (% of GB300 peak); fused sampler µs/step"
+L2_BYTES = 129 * 2 ** 20
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ---------------------------------------------------------------------------
+# bytes the step must move (algorithmic, not measured)
+# ---------------------------------------------------------------------------
+def step_bytes(w: W.Workload, out_bytes: int = 2):
+    BHD = w.B * w.H * w.D
+    L = w.seq_len.astype(np.int64)
+    self_b = int(4 * w.H * w.D * L.sum()) + BHD * 2 + BHD * out_bytes
+    if w.layout == "paged":
+        self_b += int(4 * ((L + 15) // 16).sum())
+    cross_b = int(4 * w.H * w.D * w.enc_len.astype(np.int64).sum()) + BHD * 2 + BHD * out_bytes
+    append_b = 4 * BHD * 2                                # k_new, v_new read; two rows written
+    sampler_b = w.B * w.C * w.V * 4 + w.B * w.C * 4
+    per_layer = self_b + cross_b + append_b
+    return dict(self=self_b, cross=cross_b, append=append_b, sampler=sampler_b,
+                step=w.layers * per_layer + sampler_b)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; replicas, no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float, device) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.idx = gpu_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def committed_traffic(kernel_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel_key)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "decode_attention_self_gb300", "csrc", rec["source"])
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if digest != rec.get("source_sha256_16"):
+        return None
+    return rec
+
+
+# ---------------------------------------------------------------------------
+# the step on the GPU
+# ---------------------------------------------------------------------------
+class DeviceStep:
+    def __init__(self, w: W.Workload, dev, rank: int):
+        from decode_attention_self_gb300 import api
+
+        self.api, self.w, self.dev = api, w, dev
+        self.layers = []
+        for l in range(w.layers):
+            c = W.make_self_cache(w, 1000 * rank + l, device=dev)
+            kv = api.KVCache(c.k, c.v, c.block_table.to(dev) if c.block_table is not None else None)
+            kx, vx = W.make_cross_kv(w, 1000 * rank + l, device=dev)
+            q, qx, kn, vn = W.make_step_inputs(w, 1000 * rank + l, device=dev)
+            self.layers.append(dict(kv=kv, kx=kx, vx=vx, q=q, qx=qx, kn=kn, vn=vn))
+        self.pos = torch.from_numpy(w.seq_len - 1).to(dev)
+        self.seq = torch.from_numpy(w.seq_len).to(dev)
+        self.enc = torch.from_numpy(w.enc_len).to(dev)
+        self.logits = W.make_logits(w, step_key=rank).to(dev)
+        self.seeds = torch.from_numpy(w.seeds.view(np.int64)).to(dev)
+        self.step = torch.from_numpy(w.steps.copy()).to(dev)
+        self.tokens = torch.empty((w.B, w.C), dtype=torch.int32, device=dev)
+        self.out_s = torch.empty((w.layers, w.B, w.H, w.D), dtype=torch.bfloat16, device=dev)
+        self.out_x = torch.empty_like(self.out_s)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.hint = int(w.seq_len.max())
+
+    def launches_per_step(self) -> int:
+        return 3 * self.w.layers + 1
+
+    def run(self, ev_self=None, ev_samp=None):
+        api, w = self.api, self.w
+        for l, L in enumerate(self.layers):
+            api.dr_kv_append(L["kv"], L["kn"], L["vn"], self.pos, err_flag=self.err)
+            if ev_self is not None:
+                ev_self[l][0].record()
+            api.dr_decode_self_attn(L["q"], L["kv"], self.seq, self.out_s[l], max_seq_len_hint=self.hint,
+                                    err_flag=self.err)
+            if ev_self is not None:
+                ev_self[l][1].record()
+            api.dr_decode_cross_attn(L["qx"], L["kx"], L["vx"], self.enc, self.out_x[l], err_flag=self.err)
+        if ev_samp is not None:
+            ev_samp[0].record()
+        api.dr_sample_topk_delayed(self.logits, w.temperature, w.top_k, self.seeds, self.step, w.pad_id,
+                                   self.tokens, V=w.V)
+        if ev_samp is not None:
+            ev_samp[1].record()
+
+
+class HostStep:
+    """End-to-end: the step's per-step inputs come from pinned host memory and its tokens go back to the host."""
+
+    def __init__(self, ds: DeviceStep):
+        self.ds = ds
+        self.h_in = []
+        for L in ds.layers:
+            self.h_in.append({k: L[k].cpu().pin_memory() for k in ("q", "qx", "kn", "vn")})
+        self.h_logits = ds.logits.cpu().pin_memory()
+        self.h_pos = ds.pos.cpu().pin_memory()
+        self.h_seq = ds.seq.cpu().pin_memory()
+        self.h_tokens = torch.empty_like(ds.tokens, device="cpu").pin_memory()
+        self.h2d = sum(t.numel() * t.element_size() for d in self.h_in for t in d.values()) + \
+            self.h_logits.numel() * 4 + self.h_pos.numel() * 4 + self.h_seq.numel() * 4
+        self.d2h = self.h_tokens.numel() * 4
+
+    def run(self):
+        ds = self.ds
+        for L, H in zip(ds.layers, self.h_in):
+            for k, t in H.items():
+                L[k].copy_(t, non_blocking=True)
+        ds.logits.copy_(self.h_logits, non_blocking=True)
+        ds.pos.copy_(self.h_pos, non_blocking=True)
+        ds.seq.copy_(self.h_seq, non_blocking=True)
+        ds.run()
+        self.h_tokens.copy_(ds.tokens, non_blocking=True)
+
+
+# ---------------------------------------------------------------------------
+# the oracle on a bounded sample (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """A bounded sample of one decode step for the CPU oracle: `rows` batch rows of layer 0
+    (self-attention over their paged/contiguous cache, cross-attention) and the sampler of those rows."""
+
+    def __init__(self, w: W.Workload, rows: int):
+        import oracle
+
+        self.oracle, self.w = oracle, w
+        idx = np.arange(min(rows, w.B))
+        self.sub = W.Workload(w.index, w.name, 1, len(idx), w.layout, w.seq_len[idx], w.cap, w.enc_len[idx],
+                              w.Lc_max, w.temperature, w.top_k, w.logit_std, w.seeds[idx], w.steps[idx],
+                              H=w.H, D=w.D, C=w.C, V=w.V, ldv=w.ldv, pad_id=w.pad_id, ties=w.ties)
+        s = self.sub
+        cache = W.make_self_cache(s, 0, filled_len=s.seq_len)
+        self.k, self.v = W.bits(cache.k), W.bits(cache.v)
+        self.table = cache.block_table.numpy() if cache.block_table is not None else None
+        kx, vx = W.make_cross_kv(s, 0)
+        self.kx, self.vx = W.bits(kx), W.bits(vx)
+        q, qx, _, _ = W.make_step_inputs(s, 0)
+        self.q, self.qx = W.bits(q), W.bits(qx)
+        self.logits = W.make_logits(s).numpy()
+        self.scale = 1.0 / math.sqrt(s.D)
+        b = step_bytes(s)
+        self.bytes = b["self"] + b["cross"] + b["sampler"]
+
+    def run(self, threads: int):
+        s, o = self.sub, self.oracle
+        jobs = []
+        for b in range(s.B):
+            for h in range(s.H):
+                if self.table is not None:
+                    jobs.append(lambda b=b, h=h: o.attn_paged_row(self.q[b, h], self.k, self.v, self.table[b], h,
+                                                                  int(s.seq_len[b]), self.scale))
+                else:
+                    jobs.append(lambda b=b, h=h: o.attn_contiguous_row(self.q[b, h], self.k[b, h], self.v[b, h],
+                                                                       int(s.seq_len[b]), self.scale))
+                jobs.append(lambda b=b, h=h: o.attn_contiguous_row(self.qx[b, h], self.kx[b, h], self.vx[b, h],
+                                                                   int(s.enc_len[b]), self.scale))
+            for c in range(s.C):
+                jobs.append(lambda b=b, c=c: o.sample_row(self.logits[b, c, : s.V], s.temperature, s.top_k,
+                                                          int(s.seeds[b]), b, c, int(s.steps[b]), s.pad_id))
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda f: f(), jobs))
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(w: W.Workload, steps: int, warmup: int = 0, min_seconds: float = 0.0):
+    """Time the oracle on one layer of every batch row (self + cross attention of all heads) plus the
+    sampler of every row, `steps` times (more while under min_seconds), with one thread per host core."""
+    cores = host_cores()
+    sample = OracleSample(w, w.B)
+    for _ in range(warmup):
+        sample.run(cores)
+    t0 = time.perf_counter()
+    n = 0
+    while n < steps or time.perf_counter() - t0 < min_seconds:
+        sample.run(cores)
+        n += 1
+    dt = time.perf_counter() - t0
+    gbs = sample.bytes * n / dt / 1e9
+    desc = (f"one layer of all {sample.sub.B} batch rows (self-attention over {w.layout} KV + cross-attention, "
+            f"all {w.H} heads) plus the sampler of every row and codebook, {n} repetition(s) in {dt:.1f} s, "
+            f"jobs per (row, head) and per (row, codebook) on a thread pool of {cores}")
+    return dict(value=gbs, unit="GB/s", cores=cores, kind="oracle", sample=desc,
+                seconds=dt, reps=n, bytes_per_step=sample.bytes)
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", type=int, default=5)
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+    w = W.make_workload(args.workload)
+    if args.layers > 0:
+        w = dataclasses.replace(w, layers=args.layers)
+    sb = step_bytes(w)
+    config = {"workload": f"{w.index}: {w.name}", "batch": w.B, "layers": w.layers,
+              "heads": w.H, "head_dim": w.D, "kv_layout": w.layout, "kv_dtype": "bf16", "codebooks": w.C,
+              "vocab": w.V, "top_k": w.top_k, "temperature": w.temperature,
+              "self_len_mean": float(w.seq_len.mean()), "self_len_max": int(w.seq_len.max()),
+              "cross_len_mean": float(w.enc_len.mean()), "parallelism": f"replicas x{ws}",
+              "bytes_per_step": sb["step"]}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        r = time_oracle(w, max(1, args.steps), warmup=min(args.warmup, 1))
+        steps = r["reps"]
+        ms = r["seconds"] / steps * 1e3
+        line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": ws,
+                "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+                "cpu_baseline": {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(ws, "nccl")
+    ds = DeviceStep(w, dev, rank)
+    torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        ds.run()
+    torch.cuda.synchronize()
+    assert int(ds.err.item()) == 0, "device error flag set during warm-up"
+
+    K = args.steps
+    ev_self = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(w.layers)] for _ in range(K)]
+    ev_samp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record()
+        for i in range(K):
+            ds.run(ev_self[i], ev_samp[i])
+        t1.record()
+        torch.cuda.synchronize()
+    barrier(dist)
+    ms = t0.elapsed_time(t1) / K
+    ms = max_over_ranks(dist, ms, dev)
+    self_ms = [a.elapsed_time(b) for row in ev_self for a, b in row]
+    samp_ms = [a.elapsed_time(b) for a, b in ev_samp]
+    self_avg_ms = sum(self_ms) / len(self_ms)
+    value = sb["step"] * ws / (ms * 1e-3) / 1e9
+
+    peaks, peak_kind = measured_peaks()
+    achieved = sb["self"] / (self_avg_ms * 1e-3) / 1e9
+    traffic = committed_traffic(f"decode_attn_kernel workload {w.index}")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
+                "kernel": "decode_attn_kernel (dr_decode_self_attn)", "peak_kind": peak_kind,
+                "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS, "algorithmic_bytes_per_launch": sb["self"],
+                "avg_launch_us": self_avg_ms * 1e3}
+
+    e2e = None
+    if not args.no_e2e:
+        hs = HostStep(ds)
+        for _ in range(2):
+            hs.run()
+        torch.cuda.synchronize()
+        barrier(dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            hs.run()
+        e1.record()
+        torch.cuda.synchronize()
+        ems = max_over_ranks(dist, e0.elapsed_time(e1) / K, dev)
+        e2e = {"value": sb["step"] * ws / (ems * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": hs.h2d, "d2h_bytes_per_step": hs.d2h}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        r = time_oracle(w, 1, min_seconds=10.0)
+        cpu = {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    assert int(ds.err.item()) == 0, "device error flag set during the timed steps"
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {**config, "l2": "inputs larger than L2 (%.1f GB per step vs 129 MB)" % (sb["step"] / 1e9)
+                           if sb["step"] > L2_BYTES else "inputs smaller than L2: warm-L2 figure"},
+                "us_per_step": ms * 1e3, "self_attn_us": self_avg_ms * 1e3,
+                "sampler_us": sum(samp_ms) / len(samp_ms) * 1e3,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": ds.launches_per_step() * K, "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,266 @@
+// Single-query decode attention over the valid part of a KV cache.
+//
+// Source: Optimized Parler TTS, "Analysis and improvements" -- the attention
+// kernel of a static-cache decoder must not move the whole preallocated cache
+// (~95 us) when only the valid length is needed (~13 us eager); "Future work"
+// item 1 -- a paged cache.  Cross-attention over the description encoder's
+// keys and values is the same computation on a contiguous [B][H][Lc_max][D]
+// tensor.
+//
+// Work decomposition (one launch, no workspace, no second kernel):
+//   grid = (S, H, B), one thread-block cluster of S CTAs per (b, h) row.
+//   The row's valid keys are cut into 16-key tiles (a tile is one paged
+//   block, or 2 KiB of K plus 2 KiB of V of a contiguous row); CTA s of the
+//   cluster takes an equal run of tiles, so a long row is spread over S SMs
+//   and every CTA of a cluster finishes at about the same time.
+//   Inside a CTA, warp w takes tiles w, w+4, ...; inside a warp, lane
+//   (g, e) = (lane / 8, lane % 8) owns dims 8e..8e+7 of keys g, g+4, g+8,
+//   g+12 of the tile, so each 16-byte load instruction of the warp reads
+//   512 contiguous bytes.  Each lane group keeps an fp32 online-softmax state
+//   (running max m, running sum l, acc[8]); states are merged with warp
+//   shuffles, then across warps in shared memory, then across the cluster's
+//   CTAs through distributed shared memory by CTA rank 0.
+//
+// Roofline: a key costs 256 bytes (64 bf16 of K and of V) and ~260 flops, so
+// the kernel is bound by HBM bandwidth; there is no dense contraction for the
+// tensor cores (one query row).
+#include <cooperative_groups.h>
+
+#include "dr_device.cuh"
+#include "dr_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace dr {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kD = kHeadDim;
+constexpr int kTile = kBlockKeys;
+
+struct SoftmaxPartial {
+    float m;         // max of scaled log2-domain scores
+    float l;         // sum of 2^(s - m)
+    float acc[kD];   // sum of 2^(s - m) * v
+};
+
+// Merge (m2, l2, a2) into (m, l, a); an empty state has m = -inf, l = 0, a = 0.
+template <int N>
+__device__ __forceinline__ void merge_state(float &m, float &l, float (&a)[N], float m2, float l2,
+                                            const float (&a2)[N]) {
+    const float mm = fmaxf(m, m2);
+    if (mm == -INFINITY) return;
+    const float w1 = exp2f(m - mm);
+    const float w2 = exp2f(m2 - mm);
+    l = l * w1 + l2 * w2;
+#pragma unroll
+    for (int j = 0; j < N; ++j) a[j] = a[j] * w1 + a2[j] * w2;
+    m = mm;
+}
+
+template <bool kPaged>
+__global__ void __launch_bounds__(kThreads) decode_attn_kernel(const AttnParams p) {
+    __shared__ float s_wm[kWarps], s_wl[kWarps];
+    __shared__ float s_wacc[kWarps][kD];
+    __shared__ SoftmaxPartial s_part;
+
+    const int split = blockIdx.x;
+    const int nsplit = gridDim.x;
+    const int h = blockIdx.y;
+    const int b = blockIdx.z;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int grp = lane >> 3;   // which key of each group of 4
+    const int sub = lane & 7;    // which 8 dims
+
+    int L = __ldg(p.lens + b);
+    if (L < 1 || L > p.cap) {
+        if (split == 0 && h == 0 && threadIdx.x == 0) flag_error(p.err, DR_ERRF_SEQ_LEN);
+        L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
+    }
+    const int ntiles = (L + kTile - 1) / kTile;
+    const int per = (ntiles + nsplit - 1) / nsplit;
+    const int key0 = min(split * per, ntiles) * kTile;
+    const int key1 = min(key0 + per * kTile, L);
+
+    const size_t row = (size_t)b * p.H + h;
+    float qf[8];
+    unpack8(ld_ro16(p.q + row * kD + sub * 8), qf);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) qf[j] *= p.qscale;
+
+    float m = -INFINITY, l = 0.f;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+
+    for (int t = key0 + warp * kTile; t < key1; t += kWarps * kTile) {
+        const uint16_t *kt;
+        const uint16_t *vt;
+        if constexpr (kPaged) {
+            const int blk = __ldg(p.table + (size_t)b * p.max_blocks + t / kTile);
+            if ((unsigned)blk >= (unsigned)p.num_blocks) {
+                if (lane == 0) flag_error(p.err, DR_ERRF_BLOCK_ID);
+                continue;   // warp-uniform: the whole tile is skipped
+            }
+            const size_t off = ((size_t)blk * p.H + h) * (size_t)(kTile * kD);
+            kt = p.k + off;
+            vt = p.v + off;
+        } else {
+            const size_t off = (row * (size_t)p.cap + (size_t)t) * kD;
+            kt = p.k + off;
+            vt = p.v + off;
+        }
+
+        uint4 kw[4], vw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = grp + 4 * u;
+            if (t + r < key1) {
+                kw[u] = ld_stream16(kt + r * kD + sub * 8);
+                vw[u] = ld_stream16(vt + r * kD + sub * 8);
+            } else {
+                kw[u] = make_uint4(0, 0, 0, 0);
+                vw[u] = make_uint4(0, 0, 0, 0);
+            }
+        }
+
+        float sc[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float kf[8];
+            unpack8(kw[u], kf);
+            float d = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) d = fmaf(qf[j], kf[j], d);
+            d += __shfl_xor_sync(0xFFFFFFFFu, d, 1);
+            d += __shfl_xor_sync(0xFFFFFFFFu, d, 2);
+            d += __shfl_xor_sync(0xFFFFFFFFu, d, 4);
+            sc[u] = (t + grp + 4 * u < key1) ? d : -INFINITY;
+        }
+        const float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        const float mn = fmaxf(m, mt);
+        if (mn == -INFINITY) continue;   // this lane group had no valid key yet
+        const float corr = exp2f(m - mn);
+        l *= corr;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] *= corr;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float pu = exp2f(sc[u] - mn);
+            l += pu;
+            float vf[8];
+            unpack8(vw[u], vf);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = fmaf(pu, vf[j], acc[j]);
+        }
+        m = mn;
+    }
+
+    // Lanes sub, sub+8, sub+16, sub+24 hold the same dims for different keys.
+#pragma unroll
+    for (int off = 8; off <= 16; off <<= 1) {
+        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
+        const float l2 = __shfl_xor_sync(0xFFFFFFFFu, l, off);
+        float a2[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a2[j] = __shfl_xor_sync(0xFFFFFFFFu, acc[j], off);
+        merge_state(m, l, acc, m2, l2, a2);
+    }
+    if (grp == 0) {
+        if (sub == 0) {
+            s_wm[warp] = m;
+            s_wl[warp] = l;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s_wacc[warp][sub * 8 + j] = acc[j];
+    }
+    __syncthreads();
+    if (threadIdx.x < kD) {
+        const int d = threadIdx.x;
+        float mm = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, s_wm[w]);
+        float ls = 0.f, o = 0.f;
+        if (mm != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float wt = exp2f(s_wm[w] - mm);
+                ls += wt * s_wl[w];
+                o += wt * s_wacc[w][d];
+            }
+        }
+        s_part.acc[d] = o;
+        if (d == 0) {
+            s_part.m = mm;
+            s_part.l = ls;
+        }
+    }
+
+    float *out_f = reinterpret_cast<float *>(p.out) + row * kD;
+    uint16_t *out_h = reinterpret_cast<uint16_t *>(p.out) + row * kD;
+
+    if (nsplit == 1) {
+        __syncthreads();
+        if (threadIdx.x < kD) {
+            const int d = threadIdx.x;
+            const float o = s_part.l > 0.f ? s_part.acc[d] / s_part.l : 0.f;
+            if (p.out_f32) out_f[d] = o;
+            else out_h[d] = f32_to_bf16_rn(o);
+        }
+        return;
+    }
+
+    // Cluster-wide merge of the S partial states (CTA rank == split).
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();   // every CTA's s_part is complete and visible
+    if (split == 0 && threadIdx.x < kD) {
+        const int d = threadIdx.x;
+        float mm = -INFINITY;
+        for (int r = 0; r < nsplit; ++r) {
+            const SoftmaxPartial *pr = cluster.map_shared_rank(&s_part, r);
+            mm = fmaxf(mm, pr->m);
+        }
+        float ls = 0.f, o = 0.f;
+        if (mm != -INFINITY) {
+            for (int r = 0; r < nsplit; ++r) {
+                const SoftmaxPartial *pr = cluster.map_shared_rank(&s_part, r);
+                const float wt = exp2f(pr->m - mm);
+                ls += wt * pr->l;
+                o += wt * pr->acc[d];
+            }
+        }
+        o = ls > 0.f ? o / ls : 0.f;
+        if (p.out_f32) out_f[d] = o;
+        else out_h[d] = f32_to_bf16_rn(o);
+    }
+    cluster.sync();   // keep every CTA's shared memory alive until rank 0 has read it
+}
+
+}  // namespace
+
+cudaError_t launch_decode_attn(const AttnParams &p, bool paged, int splits, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)splits, (unsigned)p.H, (unsigned)p.B);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = splits > 1 ? 1 : 0;
+    if (paged) {
+        auto kern = decode_attn_kernel<true>;
+        if (splits > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        return cudaLaunchKernelEx(&cfg, kern, p);
+    }
+    auto kern = decode_attn_kernel<false>;
+    if (splits > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace dr

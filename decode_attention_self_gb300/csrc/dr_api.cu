@@ -1,0 +1,202 @@
+// extern "C" boundary of libdecoderattn.so: argument checks, split planning
+// and launches.  Nothing here allocates device memory or synchronises with
+// the host, so every entry point can be enqueued inside CUDA-graph capture
+// (Optimized Parler TTS, "Analysis and improvements": static buffers and
+// sampling without a GPU-CPU synchronisation are what make the decode step
+// capturable as one graph).
+#include <math.h>
+
+#include <atomic>
+
+#include "dr_internal.h"
+
+namespace dr {
+
+int max_cluster_size() { return 8; }
+
+int current_device_sms() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) {
+        int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev].store(sms, std::memory_order_relaxed);
+    return sms;
+}
+
+}  // namespace dr
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates a cache description for B rows of H heads; returns the row capacity (keys) or -1.
+dr_status check_cache(const dr_kv_cache *c, int *cap) {
+    if (!c || !c->k || !c->v) return DR_ERR_INVALID_ARG;
+    if (!aligned16(c->k) || !aligned16(c->v)) return DR_ERR_INVALID_ARG;
+    if (c->reserved != 0) return DR_ERR_INVALID_ARG;
+    if (c->layout == DR_KV_CONTIGUOUS) {
+        if (c->max_len < 1) return DR_ERR_INVALID_ARG;
+        *cap = c->max_len;
+        return DR_OK;
+    }
+    if (c->layout == DR_KV_PAGED) {
+        if (!c->block_table || c->num_blocks < 1 || c->max_blocks_per_seq < 1) return DR_ERR_INVALID_ARG;
+        if (c->block_size != dr::kBlockKeys) return DR_ERR_UNSUPPORTED;
+        if ((long long)c->max_blocks_per_seq * c->block_size > 0x7FFFFFFFLL) return DR_ERR_INVALID_ARG;
+        *cap = c->max_blocks_per_seq * c->block_size;
+        return DR_OK;
+    }
+    return DR_ERR_INVALID_ARG;
+}
+
+dr_status check_dims(int B, int H, int D) {
+    if (B < 1 || H < 1 || B > 65535 || H > 65535) return DR_ERR_INVALID_ARG;
+    if (D != dr::kHeadDim) return DR_ERR_UNSUPPORTED;
+    return DR_OK;
+}
+
+dr_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DR_OK : DR_ERR_CUDA; }
+
+float softmax_scale_log2(float scale, int D) {
+    const float s = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+    return s * 1.4426950408889634f;   // log2(e): the kernel works in base 2
+}
+
+dr_status attention(const void *q, const void *k, const void *v, const int32_t *lens, const int32_t *table,
+                    bool paged, int B, int H, int cap, int max_blocks, int num_blocks, int hint, float scale,
+                    void *out, dr_dtype out_dtype, int32_t *err_flag, void *stream) {
+    if (!q || !lens || !out || !aligned16(q)) return DR_ERR_INVALID_ARG;
+    if (out_dtype != DR_BF16 && out_dtype != DR_F32) return DR_ERR_INVALID_ARG;
+    if (!(scale == scale) || isinf(scale)) return DR_ERR_INVALID_ARG;
+    const int bound = (hint > 0 && hint < cap) ? hint : cap;
+    const int sms = dr::current_device_sms();
+    if (sms <= 0) return DR_ERR_CUDA;
+    dr::AttnParams p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.k = static_cast<const uint16_t *>(k);
+    p.v = static_cast<const uint16_t *>(v);
+    p.lens = lens;
+    p.table = table;
+    p.B = B;
+    p.H = H;
+    p.cap = cap;
+    p.max_blocks = max_blocks;
+    p.num_blocks = num_blocks;
+    p.qscale = softmax_scale_log2(scale, dr::kHeadDim);
+    p.out = out;
+    p.out_f32 = out_dtype == DR_F32;
+    p.err = err_flag;
+    const int splits = dr_plan_splits(B, H, bound, sms);
+    return from_cuda(dr::launch_decode_attn(p, paged, splits, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int dr_plan_splits(int B, int H, int max_len, int num_sms) {
+    if (B < 1 || H < 1 || max_len < 1 || num_sms < 1) return 1;
+    const long long rows = (long long)B * H;
+    const int tiles = (max_len + dr::kBlockKeys - 1) / dr::kBlockKeys;
+    // At most 512 keys (32 tiles, 128 KiB of K+V) per CTA at the longest row...
+    int s = (tiles + 31) / 32;
+    // ...and at least two CTAs per SM when the batch alone cannot fill the GPU...
+    const long long fill = (2LL * num_sms + rows - 1) / rows;
+    if (fill > s) s = (int)(fill < 64 ? fill : 64);
+    // ...but never fewer than 4 tiles (64 keys) per CTA, nor more than one cluster.
+    const int by_tiles = (tiles + 3) / 4;
+    if (s > by_tiles) s = by_tiles;
+    if (s > dr::max_cluster_size()) s = dr::max_cluster_size();
+    return s < 1 ? 1 : s;
+}
+
+dr_status dr_kv_append(const dr_kv_cache *cache, const void *k_new, const void *v_new, const int32_t *pos, int B,
+                       int H, int D, int32_t *err_flag, void *stream) {
+    dr_status st = check_dims(B, H, D);
+    if (st != DR_OK) return st;
+    int cap = 0;
+    st = check_cache(cache, &cap);
+    if (st != DR_OK) return st;
+    if (!k_new || !v_new || !pos || !aligned16(k_new) || !aligned16(v_new)) return DR_ERR_INVALID_ARG;
+    dr::AppendParams p;
+    p.k = static_cast<uint16_t *>(cache->k);
+    p.v = static_cast<uint16_t *>(cache->v);
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    p.pos = pos;
+    p.table = cache->block_table;
+    p.B = B;
+    p.H = H;
+    p.cap = cap;
+    p.max_blocks = cache->max_blocks_per_seq;
+    p.num_blocks = cache->num_blocks;
+    p.err = err_flag;
+    return from_cuda(dr::launch_kv_append(p, cache->layout == DR_KV_PAGED, static_cast<cudaStream_t>(stream)));
+}
+
+dr_status dr_decode_self_attn(const void *q, const dr_kv_cache *cache, const int32_t *seq_len, int B, int H, int D,
+                              int max_seq_len_hint, float scale, void *out, dr_dtype out_dtype, int32_t *err_flag,
+                              void *stream) {
+    dr_status st = check_dims(B, H, D);
+    if (st != DR_OK) return st;
+    int cap = 0;
+    st = check_cache(cache, &cap);
+    if (st != DR_OK) return st;
+    const bool paged = cache->layout == DR_KV_PAGED;
+    return attention(q, cache->k, cache->v, seq_len, paged ? cache->block_table : nullptr, paged, B, H, cap,
+                     paged ? cache->max_blocks_per_seq : 0, paged ? cache->num_blocks : 0, max_seq_len_hint, scale,
+                     out, out_dtype, err_flag, stream);
+}
+
+dr_status dr_decode_cross_attn(const void *q, const void *k_enc, const void *v_enc, const int32_t *enc_len, int B,
+                               int H, int D, int Lc_max, float scale, void *out, dr_dtype out_dtype,
+                               int32_t *err_flag, void *stream) {
+    dr_status st = check_dims(B, H, D);
+    if (st != DR_OK) return st;
+    if (!k_enc || !v_enc || Lc_max < 1 || !aligned16(k_enc) || !aligned16(v_enc)) return DR_ERR_INVALID_ARG;
+    return attention(q, k_enc, v_enc, enc_len, nullptr, false, B, H, Lc_max, 0, 0, Lc_max, scale, out, out_dtype,
+                     err_flag, stream);
+}
+
+dr_status dr_sample_topk_delayed(const float *logits, int B, int C, int V, int ldv, float temperature, int top_k,
+                                 const uint64_t *seeds, int32_t *step, int32_t pad_id, int32_t *tokens, float *probs,
+                                 int flags, void *stream) {
+    if (!logits || !seeds || !step || !tokens) return DR_ERR_INVALID_ARG;
+    if (B < 1 || B > 0x7FFFFFFF || C < 1 || V < 1 || ldv < V) return DR_ERR_INVALID_ARG;
+    if (C > dr::kMaxCodebooks || V > dr::kMaxVocab) return DR_ERR_UNSUPPORTED;
+    if (top_k < 1 || top_k > V) return DR_ERR_INVALID_ARG;
+    if (!(temperature > 0.f) || isinf(temperature)) return DR_ERR_INVALID_ARG;
+    if (flags & ~DR_SAMPLE_ADVANCE) return DR_ERR_INVALID_ARG;
+    dr::SampleParams p;
+    p.logits = logits;
+    p.seeds = seeds;
+    p.step = step;
+    p.tokens = tokens;
+    p.probs = probs;
+    p.B = B;
+    p.C = C;
+    p.V = V;
+    p.ldv = ldv;
+    p.top_k = top_k;
+    p.pad_id = pad_id;
+    p.flags = flags;
+    p.temperature = temperature;
+    return from_cuda(dr::launch_sample(p, static_cast<cudaStream_t>(stream)));
+}
+
+const char *dr_status_string(dr_status s) {
+    switch (s) {
+        case DR_OK: return "ok";
+        case DR_ERR_INVALID_ARG: return "invalid argument";
+        case DR_ERR_UNSUPPORTED: return "unsupported shape";
+        case DR_ERR_CUDA: return "CUDA launch failed";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Internal declarations shared by the translation units of libdecoderattn.so.
+// Launch helpers take validated arguments; the extern "C" layer in dr_api.cu
+// owns all argument checking.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dr_api.h"
+
+namespace dr {
+
+constexpr int kHeadDim = 64;     // D: the only head dimension built
+constexpr int kBlockKeys = 16;   // keys per paged block, and per attention tile
+constexpr int kMaxCodebooks = 16;
+constexpr int kMaxVocab = 2048;
+
+// Largest thread-block cluster used for one (b, h) row of attention.
+int max_cluster_size();
+
+// SM count of the current device (cached per device).
+int current_device_sms();
+
+struct AttnParams {
+    const uint16_t *q;       // [B][H][64] bf16 bits
+    const uint16_t *k;       // contiguous [B][H][cap][64] or paged [NB][H][16][64]
+    const uint16_t *v;
+    const int32_t *lens;     // [B]
+    const int32_t *table;    // paged: [B][max_blocks]
+    int32_t B, H;
+    int32_t cap;             // keys a row can hold
+    int32_t max_blocks;      // paged: block-table row stride
+    int32_t num_blocks;      // paged: pool size
+    float qscale;            // softmax scale * log2(e)
+    void *out;               // [B][H][64]
+    int32_t out_f32;
+    int32_t *err;
+};
+
+cudaError_t launch_decode_attn(const AttnParams &p, bool paged, int splits, cudaStream_t stream);
+
+struct AppendParams {
+    uint16_t *k, *v;
+    const uint16_t *k_new, *v_new;   // [B][H][64]
+    const int32_t *pos;              // [B]
+    const int32_t *table;            // paged only
+    int32_t B, H, cap, max_blocks, num_blocks;
+    int32_t *err;
+};
+
+cudaError_t launch_kv_append(const AppendParams &p, bool paged, cudaStream_t stream);
+
+struct SampleParams {
+    const float *logits;     // [B][C][ldv]
+    const uint64_t *seeds;   // [B]
+    int32_t *step;           // [B]
+    int32_t *tokens;         // [B][C]
+    float *probs;            // nullable [B][C][V]
+    int32_t B, C, V, ldv, top_k, pad_id, flags;
+    float temperature;
+};
+
+cudaError_t launch_sample(const SampleParams &p, cudaStream_t stream);
+
+}  // namespace dr

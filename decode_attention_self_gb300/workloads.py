@@ -225,9 +225,9 @@ def make_logits(w: Workload, device="cpu", step_key: int = 0) -> torch.Tensor:
             order = torch.argsort(vals, descending=True, stable=True)
             kth = int(order[w.top_k - 1])
             cand = r.choice(np.setdiff1d(np.arange(w.V), [kth]), size=11, replace=False)
-            vals[cand[:2]] = vals[kth]
+            vals[cand[:2]] = float(vals[kth])
             src = r.integers(0, w.V, size=9)
-            vals[cand[2:]] = vals[src]
+            vals[cand[2:]] = vals[src].clone()
     return x.to(device)
 
 

@@ -1,0 +1,122 @@
+"""The C-ABI library loads without a GPU, exports every symbol include/dr_api.h
+declares, and rejects host-checkable mistakes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dr_api.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_attention_self_gb300 import build
+
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:dr_status|int|const char\s*\*)\s*(dr_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_decode_step_entry_points():
+    names = declared_functions()
+    for n in ("dr_kv_append", "dr_decode_self_attn", "dr_decode_cross_attn", "dr_sample_topk_delayed",
+              "dr_status_string", "dr_plan_splits"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in dr_api.h but not exported"
+
+
+def test_library_is_built_for_sm_103a_only():
+    from decode_attention_self_gb300 import build
+
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings(lib):
+    lib.dr_status_string.restype = ctypes.c_char_p
+    assert lib.dr_status_string(0) == b"ok"
+    assert lib.dr_status_string(1) == b"invalid argument"
+    assert lib.dr_status_string(2) == b"unsupported shape"
+    assert lib.dr_status_string(3) == b"CUDA launch failed"
+
+
+class Cache(ctypes.Structure):
+    _fields_ = [("layout", ctypes.c_int32), ("max_len", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("block_table", ctypes.c_void_p)]
+
+
+FAKE = 0x10000   # a 16-byte aligned non-null address; never dereferenced on the host
+
+
+def test_host_validation_rejects_before_any_launch(lib):
+    c = Cache(0, 2048, 0, 0, 0, 0, FAKE, FAKE, None)
+    cp = ctypes.byref(c)
+    vp = ctypes.c_void_p
+    # D != 64 is unsupported
+    assert lib.dr_kv_append(cp, vp(FAKE), vp(FAKE), vp(FAKE), 1, 16, 32, None, None) == 2
+    # null k_new
+    assert lib.dr_kv_append(cp, None, vp(FAKE), vp(FAKE), 1, 16, 64, None, None) == 1
+    # misaligned q
+    assert lib.dr_decode_self_attn(vp(FAKE + 2), cp, vp(FAKE), 1, 16, 64, 0, ctypes.c_float(0), vp(FAKE), 0, None,
+                                   None) == 1
+    # bad batch / heads
+    assert lib.dr_decode_self_attn(vp(FAKE), cp, vp(FAKE), 0, 16, 64, 0, ctypes.c_float(0), vp(FAKE), 0, None,
+                                   None) == 1
+    # paged with block size 32 is unsupported; paged without a table is invalid
+    cpg = Cache(1, 0, 32, 10, 4, 0, FAKE, FAKE, FAKE)
+    assert lib.dr_decode_self_attn(vp(FAKE), ctypes.byref(cpg), vp(FAKE), 1, 16, 64, 0, ctypes.c_float(0), vp(FAKE),
+                                   0, None, None) == 2
+    cpn = Cache(1, 0, 16, 10, 4, 0, FAKE, FAKE, None)
+    assert lib.dr_decode_self_attn(vp(FAKE), ctypes.byref(cpn), vp(FAKE), 1, 16, 64, 0, ctypes.c_float(0), vp(FAKE),
+                                   0, None, None) == 1
+    # unknown layout, nonzero reserved field
+    assert lib.dr_decode_self_attn(vp(FAKE), ctypes.byref(Cache(7, 16, 0, 0, 0, 0, FAKE, FAKE, None)), vp(FAKE), 1,
+                                   16, 64, 0, ctypes.c_float(0), vp(FAKE), 0, None, None) == 1
+    assert lib.dr_decode_self_attn(vp(FAKE), ctypes.byref(Cache(0, 16, 0, 0, 0, 1, FAKE, FAKE, None)), vp(FAKE), 1,
+                                   16, 64, 0, ctypes.c_float(0), vp(FAKE), 0, None, None) == 1
+    # cross attention: Lc_max < 1, bad out dtype, NaN scale
+    assert lib.dr_decode_cross_attn(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 1, 16, 64, 0, ctypes.c_float(0),
+                                    vp(FAKE), 0, None, None) == 1
+    assert lib.dr_decode_cross_attn(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 1, 16, 64, 8, ctypes.c_float(0),
+                                    vp(FAKE), 5, None, None) == 1
+    assert lib.dr_decode_cross_attn(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 1, 16, 64, 8,
+                                    ctypes.c_float(float("nan")), vp(FAKE), 0, None, None) == 1
+
+
+def test_sampler_validation(lib):
+    vp, f = ctypes.c_void_p, ctypes.c_float
+    args = lambda B=1, C=9, V=1088, ldv=1088, T=1.0, k=50, flags=0: (
+        vp(FAKE), B, C, V, ldv, f(T), k, vp(FAKE), vp(FAKE), 1024, vp(FAKE), None, flags, None)
+    assert lib.dr_sample_topk_delayed(*args(k=0)) == 1
+    assert lib.dr_sample_topk_delayed(*args(k=1089)) == 1
+    assert lib.dr_sample_topk_delayed(*args(T=0.0)) == 1
+    assert lib.dr_sample_topk_delayed(*args(T=-1.0)) == 1
+    assert lib.dr_sample_topk_delayed(*args(T=float("inf"))) == 1
+    assert lib.dr_sample_topk_delayed(*args(ldv=1000)) == 1
+    assert lib.dr_sample_topk_delayed(*args(C=17)) == 2
+    assert lib.dr_sample_topk_delayed(*args(V=4096, ldv=4096, k=5)) == 2
+    assert lib.dr_sample_topk_delayed(*args(flags=2)) == 1
+    assert lib.dr_sample_topk_delayed(vp(FAKE), 1, 9, 1088, 1088, f(1.0), 50, None, vp(FAKE), 1024, vp(FAKE), None, 0,
+                                      None) == 1
+
+
+def test_split_plan(lib):
+    # split count per (b, h) row: one cluster of at most 8 CTAs, >= 64 keys each, <= 512 keys each at
+    # the longest row when possible, and enough CTAs to cover a 152-SM GPU twice at small batch.
+    plan = lib.dr_plan_splits
+    assert plan(128, 16, 4096, 152) == 8      # batch 128, rows up to 4096 keys: 512 keys per CTA
+    assert plan(32, 16, 2048, 152) == 4       # batch 32, rows up to 2048 keys
+    assert plan(1, 16, 1024, 152) == 8        # batch 1: fill the GPU, capped by the cluster size
+    assert plan(1, 16, 64, 152) == 1          # a 64-key row is one CTA
+    assert plan(1, 16, 200, 152) == 4         # 13 tiles, at least 4 per CTA: ceil(13 / 4) = 4 CTAs

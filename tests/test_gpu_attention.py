@@ -1,0 +1,270 @@
+"""GPU parity of dr_decode_self_attn / dr_decode_cross_attn against the oracle.
+
+Single-query attention over the valid part of a static or paged cache
+(Optimized Parler TTS, "Analysis and improvements" and "Future work" item 1)
+and over the description encoder's keys and values (architecture overview).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_attention_self_gb300 import workloads as W
+from tests.parity import assert_attn_close, default_scale
+
+pytestmark = pytest.mark.gpu
+
+D = 64
+
+
+@pytest.fixture(scope="module")
+def api(cuda_device):
+    from decode_attention_self_gb300 import api as _api
+
+    return _api
+
+
+def to_dev(cache: W.SelfCache, dev):
+    from decode_attention_self_gb300 import api as _api
+
+    return _api.KVCache(cache.k.to(dev), cache.v.to(dev),
+                        cache.block_table.to(dev) if cache.block_table is not None else None)
+
+
+def oracle_self(w, cache, q, scale, lens=None):
+    lens = w.seq_len if lens is None else lens
+    if cache.layout == "contiguous":
+        return oracle.attn_contiguous(W.bits(q), W.bits(cache.k), W.bits(cache.v), lens, scale)
+    return oracle.attn_paged(W.bits(q), W.bits(cache.k), W.bits(cache.v), cache.block_table.numpy(), lens, scale)
+
+
+# ---------------------------------------------------------------------------
+# the five workloads: append + self-attention + cross-attention of one layer
+# ---------------------------------------------------------------------------
+_HOST = {}
+
+
+def host_layer(index):
+    """Seeded host inputs of one layer of workload `index` (generated once per module)."""
+    if index not in _HOST:
+        w = W.make_workload(index)
+        layer = 0 if index != 2 else 7
+        cache = W.make_self_cache(w, layer)                   # slot seq_len-1 is NaN until the append
+        _HOST[index] = (w, cache, W.make_step_inputs(w, layer), W.make_cross_kv(w, layer))
+    return _HOST[index]
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_workload_layer_parity(api, cuda_device, index, out_dtype):
+    dev = cuda_device
+    w, cache, (q, qx, kn, vn), (kx, vx) = host_layer(index)
+    kv = to_dev(cache, dev)
+    pos = torch.from_numpy(w.seq_len - 1).to(dev)
+    seq = torch.from_numpy(w.seq_len).to(dev)
+    enc = torch.from_numpy(w.enc_len).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out_s = torch.empty((w.B, w.H, D), dtype=out_dtype, device=dev)
+    out_x = torch.empty_like(out_s)
+    api.dr_kv_append(kv, kn.to(dev), vn.to(dev), pos, err_flag=err)
+    api.dr_decode_self_attn(q.to(dev), kv, seq, out_s, max_seq_len_hint=int(w.seq_len.max()), err_flag=err)
+    api.dr_decode_cross_attn(qx.to(dev), kx.to(dev), vx.to(dev), enc, out_x, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+    scale = default_scale(D)
+    kh, vh = W.bits(cache.k).copy(), W.bits(cache.v).copy()
+    if cache.layout == "contiguous":
+        oracle.kv_append_contiguous(kh, vh, W.bits(kn), W.bits(vn), w.seq_len - 1)
+        ref_s = oracle.attn_contiguous(W.bits(q), kh, vh, w.seq_len, scale)
+    else:
+        table = cache.block_table.numpy()
+        oracle.kv_append_paged(kh, vh, table, W.bits(kn), W.bits(vn), w.seq_len - 1)
+        ref_s = oracle.attn_paged(W.bits(q), kh, vh, table, w.seq_len, scale)
+    ref_x = oracle.attn_contiguous(W.bits(qx), W.bits(kx), W.bits(vx), w.enc_len, scale)
+    assert_attn_close(out_s, ref_s, f"self-attention, workload {index}")
+    assert_attn_close(out_x, ref_x, f"cross-attention, workload {index}")
+    # the append wrote exactly the new rows (bit-exact cache contents)
+    assert np.array_equal(W.bits(kv.k), kh) and np.array_equal(W.bits(kv.v), vh)
+
+
+# ---------------------------------------------------------------------------
+# edge cases: lengths around tile boundaries, capacity, every split count
+# ---------------------------------------------------------------------------
+LENS = [1, 2, 15, 16, 17, 31, 33, 63, 64, 65, 100, 255, 256]
+
+
+def ragged_case(layout, lens, cap, H=16, seed=0):
+    w = W.Workload(100 + seed, "edge", 1, len(lens), layout, np.array(lens, np.int32), cap,
+                   np.array(lens, np.int32), cap, 1.0, 1, 1.0, np.zeros(len(lens), np.uint64),
+                   np.zeros(len(lens), np.int32), H=H)
+    cache = W.make_self_cache(w, seed, filled_len=w.seq_len)
+    q = W.randn_bf16((w.B, H, D), "cpu", 100 + seed, 9)
+    return w, cache, q
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+@pytest.mark.parametrize("hint", [0, 64, 256, 1024])
+def test_ragged_lengths_and_split_counts(api, cuda_device, layout, hint):
+    w, cache, q = ragged_case(layout, LENS, 256)
+    kv = to_dev(cache, cuda_device)
+    out = torch.empty((w.B, w.H, D), dtype=torch.float32, device=cuda_device)
+    api.dr_decode_self_attn(q.to(cuda_device), kv, torch.from_numpy(w.seq_len).to(cuda_device), out,
+                            max_seq_len_hint=hint)
+    assert_attn_close(out, oracle_self(w, cache, q, default_scale(D)), f"{layout} hint {hint}")
+
+
+@pytest.mark.parametrize("L", [1, 17, 1000, 4095, 4096])
+def test_batch1_long_rows(api, cuda_device, L):
+    w, cache, q = ragged_case("contiguous", [L], 4096, seed=3)
+    kv = to_dev(cache, cuda_device)
+    out = torch.empty((1, 16, D), dtype=torch.float32, device=cuda_device)
+    api.dr_decode_self_attn(q.to(cuda_device), kv, torch.from_numpy(w.seq_len).to(cuda_device), out)
+    assert_attn_close(out, oracle_self(w, cache, q, default_scale(D)), f"L={L}")
+
+
+def test_other_head_counts_and_scale(api, cuda_device):
+    for H in (1, 3, 40):
+        w, cache, q = ragged_case("paged", [5, 70, 129], 160, H=H, seed=H)
+        kv = to_dev(cache, cuda_device)
+        out = torch.empty((w.B, H, D), dtype=torch.float32, device=cuda_device)
+        api.dr_decode_self_attn(q.to(cuda_device), kv, torch.from_numpy(w.seq_len).to(cuda_device), out, scale=0.3)
+        assert_attn_close(out, oracle_self(w, cache, q, 0.3), f"H={H}")
+
+
+def test_paged_equals_contiguous_bitwise(api, cuda_device):
+    # Same logical rows, same split plan: the kernel's reduction order depends only on the tile
+    # partition, so the paged layout with a shuffled table must reproduce the contiguous result bit for bit.
+    lens = [7, 16, 100, 255, 256, 33]
+    wc, cc, q = ragged_case("contiguous", lens, 256, seed=5)
+    wp = W.Workload(105, "edge", 1, len(lens), "paged", wc.seq_len, 256, wc.seq_len, 256, 1.0, 1, 1.0,
+                    wc.seeds, wc.steps)
+    table, NB = W.make_block_table(wp, "cpu", 5)
+    kp = torch.full((NB, 16, 16, D), float("nan"), dtype=torch.bfloat16)
+    vp = kp.clone()
+    for b, L in enumerate(lens):
+        for j in range((L + 15) // 16):
+            kp[table[b, j]] = cc.k[b, :, 16 * j:16 * j + 16]
+            vp[table[b, j]] = cc.v[b, :, 16 * j:16 * j + 16]
+    from decode_attention_self_gb300 import api as _api
+    dev = cuda_device
+    kvc = _api.KVCache(cc.k.to(dev), cc.v.to(dev))
+    kvp = _api.KVCache(kp.to(dev), vp.to(dev), table.to(dev))
+    seq = torch.from_numpy(wc.seq_len).to(dev)
+    oc = torch.empty((len(lens), 16, D), dtype=torch.float32, device=dev)
+    op = torch.empty_like(oc)
+    for hint in (0, 64, 256):
+        api.dr_decode_self_attn(q.to(dev), kvc, seq, oc, max_seq_len_hint=hint)
+        api.dr_decode_self_attn(q.to(dev), kvp, seq, op, max_seq_len_hint=hint)
+        torch.cuda.synchronize()
+        assert torch.equal(oc, op), f"hint {hint}"
+
+
+def test_deterministic_and_batch_position_invariant(api, cuda_device):
+    lens = [300, 12, 1024, 77, 513, 5, 1000, 64] * 5          # 40 rows: the split plan is set by the length
+    w, cache, q = ragged_case("paged", lens, 1024, seed=7)
+    dev = cuda_device
+    kv = to_dev(cache, dev)
+    seq = torch.from_numpy(w.seq_len).to(dev)
+    o1 = torch.empty((w.B, 16, D), dtype=torch.float32, device=dev)
+    o2 = torch.empty_like(o1)
+    api.dr_decode_self_attn(q.to(dev), kv, seq, o1)
+    api.dr_decode_self_attn(q.to(dev), kv, seq, o2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+    perm = torch.from_numpy(np.random.default_rng(8).permutation(w.B))
+    kvp = type(kv)(kv.k, kv.v, kv.block_table[perm.to(dev)].contiguous())
+    o3 = torch.empty_like(o1)
+    api.dr_decode_self_attn(q[perm].contiguous().to(dev), kvp, seq[perm.to(dev)].contiguous(), o3)
+    torch.cuda.synchronize()
+    assert torch.equal(o3, o1[perm.to(dev)])
+
+
+def test_cross_attention_ragged_lengths(api, cuda_device):
+    B, H, Lc = 6, 16, 300
+    enc_len = np.array([1, 16, 17, 150, 299, 300], np.int32)
+    w = W.Workload(110, "cross", 1, B, "contiguous", enc_len, Lc, enc_len, Lc, 1.0, 1, 1.0, np.zeros(B, np.uint64),
+                   np.zeros(B, np.int32))
+    kx, vx = W.make_cross_kv(w, 0)
+    q = W.randn_bf16((B, H, D), "cpu", 110, 1)
+    dev = cuda_device
+    for out_dtype in (torch.float32, torch.bfloat16):
+        out = torch.empty((B, H, D), dtype=out_dtype, device=dev)
+        api.dr_decode_cross_attn(q.to(dev), kx.to(dev), vx.to(dev), torch.from_numpy(enc_len).to(dev), out)
+        ref = oracle.attn_contiguous(W.bits(q), W.bits(kx), W.bits(vx), enc_len, default_scale(D))
+        assert_attn_close(out, ref, f"cross {out_dtype}")
+
+
+# ---------------------------------------------------------------------------
+# device-side errors: flagged, clamped or skipped, never a trap
+# ---------------------------------------------------------------------------
+def test_length_above_capacity_is_clamped_and_flagged(api, cuda_device):
+    w, cache, q = ragged_case("contiguous", [64, 64], 64, seed=9)
+    dev = cuda_device
+    kv = to_dev(cache, dev)
+    seq = torch.tensor([64, 500], dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty((2, 16, D), dtype=torch.float32, device=dev)
+    api.dr_decode_self_attn(q.to(dev), kv, seq, out, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 1
+    assert_attn_close(out, oracle_self(w, cache, q, default_scale(D), lens=np.array([64, 64], np.int32)))
+
+
+def test_zero_length_row_outputs_zeros_and_is_flagged(api, cuda_device):
+    w, cache, q = ragged_case("contiguous", [10, 10], 64, seed=10)
+    dev = cuda_device
+    kv = to_dev(cache, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.full((2, 16, D), 7.0, dtype=torch.float32, device=dev)
+    api.dr_decode_self_attn(q.to(dev), kv, torch.tensor([10, 0], dtype=torch.int32, device=dev), out, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 1
+    assert torch.count_nonzero(out[1]) == 0
+    assert_attn_close(out[0:1], oracle_self(w, cache, q, default_scale(D))[0:1])
+
+
+def test_block_id_outside_pool_is_skipped_and_flagged(api, cuda_device):
+    w, cache, q = ragged_case("paged", [40], 64, seed=11)
+    dev = cuda_device
+    table = cache.block_table.clone()
+    table[0, 1] = cache.num_blocks + 1000          # never dereferenced: the kernel checks it first
+    from decode_attention_self_gb300 import api as _api
+    kv = _api.KVCache(cache.k.to(dev), cache.v.to(dev), table.to(dev))
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty((1, 16, D), dtype=torch.float32, device=dev)
+    api.dr_decode_self_attn(q.to(dev), kv, torch.tensor([40], dtype=torch.int32, device=dev), out, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 2
+    # keys 16..31 were skipped: the result is attention over keys 0..15 and 32..39
+    kb, vb = W.bits(cache.k), W.bits(cache.v)
+    t = cache.block_table.numpy()[0]
+    keep = [(t[j // 16], j % 16) for j in list(range(16)) + list(range(32, 40))]
+    ref = np.zeros((1, 16, D))
+    for h in range(16):
+        ks = np.stack([kb[blk, h, s] for blk, s in keep])
+        vs = np.stack([vb[blk, h, s] for blk, s in keep])
+        ref[0, h] = oracle.attend(W.bits(q)[0, h], ks, vs, default_scale(D))[0]
+    assert_attn_close(out, ref)
+
+
+def test_calls_capture_into_a_cuda_graph(api, cuda_device):
+    w, cache, q = ragged_case("paged", [33, 200, 256], 256, seed=12)
+    dev = cuda_device
+    kv = to_dev(cache, dev)
+    seq = torch.from_numpy(w.seq_len).to(dev)
+    qd = q.to(dev)
+    out_e = torch.empty((w.B, 16, D), dtype=torch.float32, device=dev)
+    out_g = torch.empty_like(out_e)
+    api.dr_decode_self_attn(qd, kv, seq, out_e)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            api.dr_decode_self_attn(qd, kv, seq, out_g)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_e, out_g)

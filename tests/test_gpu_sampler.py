@@ -1,0 +1,165 @@
+"""GPU parity of dr_sample_topk_delayed against the oracle.
+
+The fused sampler (Optimized Parler TTS, "Future work" item 2: temperature,
+top-k and softmax in one kernel; the nine codebooks under the delayed pattern,
+architecture overview): tokens bit-exact outside the Gumbel-margin exclusion,
+top-k sets bit-exact (ties to the lower index), probabilities within fp32
+tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_attention_self_gb300 import workloads as W
+from tests.parity import assert_probs_match, assert_tokens_match
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api(cuda_device):
+    from decode_attention_self_gb300 import api as _api
+
+    return _api
+
+
+def run_gpu(api, dev, logits, T, k, seeds, steps, pad_id, V=None, want_probs=True, advance=False):
+    B, C, ldv = logits.shape
+    V = ldv if V is None else V
+    lg = torch.as_tensor(logits).to(dev)
+    sd = torch.from_numpy(np.asarray(seeds, np.uint64).view(np.int64)).to(dev)
+    st = torch.from_numpy(np.asarray(steps, np.int32).copy()).to(dev)
+    tok = torch.full((B, C), -7, dtype=torch.int32, device=dev)
+    pr = torch.full((B, C, V), -1.0, dtype=torch.float32, device=dev) if want_probs else None
+    api.dr_sample_topk_delayed(lg, T, k, sd, st, pad_id, tok, pr, V=V, advance=advance)
+    torch.cuda.synchronize()
+    return tok, pr, st
+
+
+def check(api, dev, logits, T, k, seeds, steps, pad_id, V=None):
+    x = np.asarray(logits, np.float32)
+    tok, pr, _ = run_gpu(api, dev, x, T, k, seeds, steps, pad_id, V=V)
+    ref = oracle.sample(x, T, k, seeds, steps, pad_id, V=V, want_probs=True)
+    n_cmp, n_excl = assert_tokens_match(tok, ref)
+    assert_probs_match(pr, ref)
+    return n_cmp, n_excl
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+def test_workload_sampler_parity(api, cuda_device, index):
+    w = W.make_workload(index)
+    logits = W.make_logits(w).numpy()
+    n_cmp, n_excl = check(api, cuda_device, logits, w.temperature, w.top_k, w.seeds, w.steps, w.pad_id, V=w.V)
+    assert n_cmp > 0 and n_excl <= max(1, n_cmp // 100)
+
+
+def test_many_steps_and_seeds(api, cuda_device):
+    rng = np.random.default_rng(1)
+    B = 64
+    logits = (rng.normal(size=(B, 9, 1088)) * 3).astype(np.float32)
+    seeds = rng.integers(0, 2 ** 63, size=B, dtype=np.uint64) * np.uint64(2) + np.uint64(1)
+    steps = rng.integers(0, 5000, size=B).astype(np.int32)
+    check(api, cuda_device, logits, 1.0, 50, seeds, steps, 1024)
+
+
+@pytest.mark.parametrize("V", [1, 5, 64, 65, 256, 257, 512, 513, 1088, 1089, 2048])
+def test_vocab_sizes(api, cuda_device, V):
+    rng = np.random.default_rng(V)
+    logits = (rng.normal(size=(3, 9, V)) * 2).astype(np.float32)
+    for k in sorted({1, min(V, 7), min(V, 50), V}):
+        check(api, cuda_device, logits, 0.9, k, np.array([5, 6, 7], np.uint64), np.array([9, 9, 9], np.int32), 3)
+
+
+@pytest.mark.parametrize("C", [1, 4, 9, 16])
+def test_codebook_counts(api, cuda_device, C):
+    rng = np.random.default_rng(C)
+    logits = (rng.normal(size=(2, C, 300)) * 3).astype(np.float32)
+    check(api, cuda_device, logits, 1.3, 20, np.array([1, 2], np.uint64), np.array([C + 1, C // 2], np.int32), 7)
+
+
+def test_row_stride_padding_is_never_read(api, cuda_device):
+    rng = np.random.default_rng(2)
+    x = np.full((4, 9, 1096), np.nan, np.float32)
+    x[:, :, :1088] = rng.normal(size=(4, 9, 1088)) * 3
+    check(api, cuda_device, x, 1.0, 50, np.arange(4, dtype=np.uint64), np.full(4, 20, np.int32), 1024, V=1088)
+
+
+def test_planted_ties_at_the_topk_boundary(api, cuda_device):
+    rng = np.random.default_rng(3)
+    B, V, k = 16, 1088, 250
+    x = (rng.normal(size=(B, 9, V)) * 5).astype(np.float32)
+    for b in range(B):
+        for c in range(9):
+            row = x[b, c]
+            kth = np.argsort(-row, kind="stable")[k - 1]
+            idx = rng.choice(V, size=20, replace=False)
+            row[idx] = row[kth]                        # 21 entries share the boundary value
+    check(api, cuda_device, x, 0.7, k, np.arange(B, dtype=np.uint64) + 99, np.full(B, 15, np.int32), 1024)
+
+
+def test_all_equal_logits_take_the_first_k(api, cuda_device):
+    x = np.zeros((2, 9, 1088), np.float32)
+    tok, pr, _ = run_gpu(api, cuda_device, x, 1.0, 50, np.array([1, 2], np.uint64), np.array([20, 20], np.int32), 5)
+    support = (pr.cpu().numpy() != 0)
+    assert (support[:, :, :50]).all() and not support[:, :, 50:].any()
+    check(api, cuda_device, x, 1.0, 50, np.array([1, 2], np.uint64), np.array([20, 20], np.int32), 5)
+
+
+def test_negative_infinity_logits(api, cuda_device):
+    rng = np.random.default_rng(4)
+    x = (rng.normal(size=(3, 9, 200)) * 2).astype(np.float32)
+    x[0, :, :] = -np.inf                               # whole rows -inf: the lowest index of the set
+    x[1, :, 150:] = -np.inf                            # k larger than the finite count
+    x[2, :, ::3] = -np.inf
+    check(api, cuda_device, x, 1.0, 170, np.array([1, 2, 3], np.uint64), np.full(3, 12, np.int32), 9)
+    check(api, cuda_device, x, 1.0, 1, np.array([1, 2, 3], np.uint64), np.full(3, 12, np.int32), 9)
+
+
+def test_k1_is_argmax(api, cuda_device):
+    rng = np.random.default_rng(5)
+    x = rng.integers(-4, 4, size=(8, 9, 1088)).astype(np.float32)   # many exact ties
+    tok, _, _ = run_gpu(api, cuda_device, x, 1.0, 1, np.arange(8, dtype=np.uint64), np.full(8, 50, np.int32), 0)
+    assert np.array_equal(tok.cpu().numpy(), x.argmax(axis=2))
+
+
+@pytest.mark.parametrize("step", list(range(0, 11)))
+def test_delay_pattern(api, cuda_device, step):
+    rng = np.random.default_rng(step)
+    x = (rng.normal(size=(2, 9, 1088)) * 3).astype(np.float32)
+    x[:, :, 1024] = -np.inf
+    tok, pr, _ = run_gpu(api, cuda_device, x, 1.0, 50, np.array([0, 1], np.uint64), np.array([step, step], np.int32),
+                         1024)
+    t = tok.cpu().numpy()
+    for c in range(9):
+        assert ((t[:, c] == 1024) == (step <= c)).all()
+        if step <= c:
+            assert (pr[:, c].cpu().numpy() == 0).all()
+    check(api, cuda_device, x, 1.0, 50, np.array([0, 1], np.uint64), np.array([step, step], np.int32), 1024)
+
+
+def test_advance_flag_increments_step_once_per_call(api, cuda_device):
+    rng = np.random.default_rng(6)
+    B = 5
+    x = (rng.normal(size=(B, 9, 1088)) * 3).astype(np.float32)
+    steps0 = np.array([0, 3, 8, 9, 100], np.int32)
+    seeds = np.arange(B, dtype=np.uint64)
+    dev = cuda_device
+    lg = torch.from_numpy(x).to(dev)
+    sd = torch.from_numpy(seeds.view(np.int64)).to(dev)
+    st = torch.from_numpy(steps0.copy()).to(dev)
+    tok = torch.empty((B, 9), dtype=torch.int32, device=dev)
+    for it in range(3):
+        api.dr_sample_topk_delayed(lg, 1.0, 50, sd, st, 1024, tok, advance=True)
+        torch.cuda.synchronize()
+        ref = oracle.sample(x, 1.0, 50, seeds, steps0 + it, 1024)
+        assert_tokens_match(tok, ref)
+        assert np.array_equal(st.cpu().numpy(), steps0 + it + 1)
+
+
+def test_deterministic(api, cuda_device):
+    w = W.make_workload(5)
+    x = W.make_logits(w).numpy()
+    a, pa, _ = run_gpu(api, cuda_device, x, w.temperature, w.top_k, w.seeds, w.steps, w.pad_id)
+    b, pb, _ = run_gpu(api, cuda_device, x, w.temperature, w.top_k, w.seeds, w.steps, w.pad_id)
+    assert torch.equal(a, b) and torch.equal(pa, pb)
