@@ -334,6 +334,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch the timed steps one by one instead of a CUDA graph")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     w = W.make_workload(args.workload)
@@ -374,17 +375,42 @@ def main():
     torch.cuda.synchronize()
     assert int(ds.err.item()) == 0, "device error flag set during warm-up"
 
+    # The timed region is K decode steps.  By default they are captured as one CUDA graph
+    # (the page's own way of removing launch overhead), with event nodes around every
+    # self-attention and sampler launch; --eager launches them one by one instead.
     K = args.steps
-    ev_self = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(w.layers)] for _ in range(K)]
-    ev_samp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    mode = "eager" if args.eager else "cuda_graph"
+    graph = None
+    if not args.eager:
+        try:
+            mk = lambda: torch.cuda.Event(enable_timing=True, external=True)
+            ev_self = [[(mk(), mk()) for _ in range(w.layers)] for _ in range(K)]
+            ev_samp = [(mk(), mk()) for _ in range(K)]
+            graph = torch.cuda.CUDAGraph()
+            cs = torch.cuda.Stream()
+            cs.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(graph, stream=cs):
+                for i in range(K):
+                    ds.run(ev_self[i], ev_samp[i])
+            torch.cuda.current_stream().wait_stream(cs)
+            graph.replay()                                 # untimed: instantiation and first-touch costs
+            torch.cuda.synchronize()
+        except TypeError:                                  # a torch without external (graph-node) events
+            graph, mode = None, "eager"
+    if graph is None:
+        mk = lambda: torch.cuda.Event(enable_timing=True)
+        ev_self = [[(mk(), mk()) for _ in range(w.layers)] for _ in range(K)]
+        ev_samp = [(mk(), mk()) for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t0.record()
-        for i in range(K):
-            ds.run(ev_self[i], ev_samp[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(K):
+                ds.run(ev_self[i], ev_samp[i])
         t1.record()
         torch.cuda.synchronize()
     barrier(dist)
@@ -436,7 +462,7 @@ def main():
                 "us_per_step": ms * 1e3, "self_attn_us": self_avg_ms * 1e3,
                 "sampler_us": sum(samp_ms) / len(samp_ms) * 1e3,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": ds.launches_per_step() * K, "clocks": clk.summary()}
+                "gpu_launches": ds.launches_per_step() * K, "launch_mode": mode, "clocks": clk.summary()}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -7,33 +7,40 @@
 // sampling without a GPU-CPU synchronisation; the architecture overview --
 // nine DAC codebooks, one token each per step, in a delayed pattern.
 //
-// One CTA per batch row b; inside it one group of 64 threads (two warps) per
-// codebook c.  A group
-//   1. reads its V logits once into registers, divides by T with IEEE
-//      round-to-nearest and maps each float to an order-preserving uint32 key;
-//   2. finds the k-th largest key tau by a 4-pass, 8-bit radix select over
-//      shared-memory histograms (no sort, no second read of the logits);
-//   3. takes every key > tau plus the lowest-index entries equal to tau
-//      (their rank in index order comes from warp ballots), so ties go to the
-//      lower index exactly;
-//   4. draws by Gumbel-max over that set: u from Philox4x32-10 (Salmon et
-//      al., SC'11) keyed by the row's seed, counter (i/4, c, step, b), then
-//      argmax of x_i - log(-log u_i), equal scores to the lower index;
-//   5. optionally writes softmax probabilities over the set.
-// Codebooks c with step[b] <= c emit pad_id (delay pattern).  With DR_SAMPLE_ADVANCE, thread 0 increments
-// step[b] after a CTA-wide barrier, when every group has read it.
+// Grid (C, B): one CTA of 256 threads per (codebook c, row b).  A CTA
+//   1. reads its V logits once (element i = t + 256 j stays in thread t's
+//      registers), divides by T with IEEE round-to-nearest and maps each float
+//      to an order-preserving uint32 key;
+//   2. finds the top_k-th largest key tau by a 4-pass, 8-bit radix select:
+//      shared-memory histograms filled with warp-aggregated atomics (lanes
+//      holding the same digit add once), scanned in descending digit order;
+//   3. keeps every key > tau plus the lowest-index entries equal to tau (their
+//      rank in index order comes from warp ballots), so ties go to the lower
+//      index exactly, and compacts the kept indices into a shared list;
+//   4. draws by Gumbel-max over the list, spread evenly over the threads:
+//      u_i from Philox4x32-10 (Salmon et al., SC'11) keyed by the row's seed,
+//      counter (i/4, c, step, b); argmax of x_i - log(-log u_i), equal scores
+//      to the lower index;
+//   5. optionally writes the softmax over the kept set.
+// A codebook with step[b] <= c emits pad_id (delay pattern).  With
+// DR_SAMPLE_ADVANCE the C CTAs of a row form one thread-block cluster; after a
+// cluster barrier -- every CTA has read step[b] -- rank 0 increments it.
 //
-// Latency-bound: 39 KB of logits per row at B = 1 is nanoseconds of HBM
-// time; the cost is the dependent passes, kept on-chip.
+// Latency-bound: the 39 KB of logits of a row are nanoseconds of HBM time; the
+// cost is the chain of dependent on-chip passes.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "dr_device.cuh"
 #include "dr_internal.h"
 
+namespace cg = cooperative_groups;
+
 namespace dr {
 namespace {
 
-constexpr int kGroup = 64;   // threads per codebook
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 
 // Philox4x32-10, Salmon, Moraes, Dror and Shaw, SC'11, section 3.
 __device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1) {
@@ -64,140 +71,168 @@ __device__ __forceinline__ bool better(float s, int i, float bs, int bi) {
     return s > bs || (s == bs && i < bi);
 }
 
-template <int EPT>
-__global__ void __launch_bounds__(kMaxCodebooks *kGroup) sample_kernel(const SampleParams p) {
-    __shared__ uint32_t s_hist[kMaxCodebooks][256];
-    __shared__ uint32_t s_bal[kMaxCodebooks][EPT][2];
-    __shared__ uint32_t s_scan[kMaxCodebooks][2];
-    __shared__ int s_sel[kMaxCodebooks][2];
-    __shared__ float s_rf[kMaxCodebooks][2];
-    __shared__ int s_ri[kMaxCodebooks][2];
-
-    const int b = blockIdx.x;
-    const int c = threadIdx.x / kGroup;
-    const int t = threadIdx.x % kGroup;
-    const int wg = t >> 5;
-    const int lane = threadIdx.x & 31;
-    const int step = p.step[b];
-    const uint64_t seed = p.seeds[b];
-    const bool active = step > c;   // delay pattern: codebook c is padded while step <= c
-    const float *row = p.logits + ((size_t)b * p.C + c) * (size_t)p.ldv;
-
-    // Only the order keys stay in registers; key_value() inverts the map.
-    uint32_t key[EPT];
-    uint32_t valid = 0;
+// Block-wide exclusive prefix sum of one value per thread (all threads call).
+__device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
 #pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-        const int i = t + kGroup * j;
-        key[j] = 0u;
-        if (active && i < p.V) {
-            key[j] = order_key(__fdiv_rn(__ldg(row + i), p.temperature));
-            valid |= 1u << j;
-        }
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += n;
     }
-
-    // ---- radix select of the top_k-th largest key -------------------------
-    uint32_t prefix = 0u, pmask = 0u;
-    int kk = p.top_k;
-    uint32_t inc = 0u, tot = 0u;
-#pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        for (int q = t; q < 256; q += kGroup) s_hist[c][q] = 0u;
-        __syncthreads();
-        if (active) {
+    if (lane == 31) s_warp[warp] = inc;
+    __syncthreads();
+    int before = 0;
+    total = 0;
 #pragma unroll
-            for (int j = 0; j < EPT; ++j)
-                if (((valid >> j) & 1u) && (key[j] & pmask) == prefix)
-                    atomicAdd(&s_hist[c][(key[j] >> shift) & 255u], 1u);
+    for (int w = 0; w < kWarps; ++w) {
+        const int s = s_warp[w];
+        if (w < warp) before += s;
+        total += s;
+    }
+    __syncthreads();   // s_warp may be reused right after
+    return before + inc - v;
+}
+
+template <int EPT>
+__global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) {
+    __shared__ uint32_t s_hist[2][256];
+    __shared__ uint32_t s_wtot[kWarps];
+    __shared__ int s_sel[2];
+    __shared__ uint32_t s_bal[EPT][kWarps];
+    __shared__ int s_scan[kWarps];
+    __shared__ int s_list[kMaxVocab];
+    __shared__ float s_rf[kWarps];
+    __shared__ int s_ri[kWarps];
+
+    const int c = blockIdx.x;
+    const int b = blockIdx.y;
+    const int t = threadIdx.x;
+    const int lane = t & 31, warp = t >> 5;
+    const int step = p.step[b];
+    const bool active = step > c;   // delay pattern: codebook c is padded while step <= c
+    float *prow = p.probs ? p.probs + ((size_t)b * p.C + c) * (size_t)p.V : nullptr;
+
+    if (!active) {
+        if (t == 0) p.tokens[(size_t)b * p.C + c] = p.pad_id;
+        if (prow)
+            for (int i = t; i < p.V; i += kThreads) prow[i] = 0.f;
+    } else {
+        const float *row = p.logits + ((size_t)b * p.C + c) * (size_t)p.ldv;
+        // Only the order keys stay in registers; key_value() inverts the map.
+        uint32_t key[EPT];
+        uint32_t valid = 0;
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+            const int i = t + kThreads * j;
+            key[j] = 0u;
+            if (i < p.V) {
+                key[j] = order_key(__fdiv_rn(__ldg(row + i), p.temperature));
+                valid |= 1u << j;
+            }
         }
+        s_hist[0][t] = 0u;
+        s_hist[1][t] = 0u;
         __syncthreads();
-        if (active) {
-            // thread t owns bins 255-4t .. 252-4t, i.e. descending digit order
-            const int top = 255 - 4 * t;
-            tot = s_hist[c][top] + s_hist[c][top - 1] + s_hist[c][top - 2] + s_hist[c][top - 3];
-            inc = tot;
+
+        // ---- radix select of the top_k-th largest key ------------------------
+        uint32_t prefix = 0u, pmask = 0u;
+        int kk = p.top_k;
+#pragma unroll 1
+        for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            uint32_t *hist = s_hist[pass & 1];
+#pragma unroll
+            for (int j = 0; j < EPT; ++j) {
+                const bool in = ((valid >> j) & 1u) && (key[j] & pmask) == prefix;
+                const uint32_t digit = in ? (key[j] >> shift) & 255u : 0x100u;
+                const uint32_t peers = __match_any_sync(0xFFFFFFFFu, digit);
+                if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+            }
+            __syncthreads();
+            // thread t owns digit 255 - t: an inclusive scan over t walks digits downward
+            const uint32_t cnt = hist[255 - t];
+            uint32_t inc = cnt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const uint32_t n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
                 if (lane >= o) inc += n;
             }
-            if (lane == 31) s_scan[c][wg] = inc;
-        }
-        __syncthreads();
-        if (active) {
-            const uint32_t before = inc - tot + (wg ? s_scan[c][0] : 0u);
-            if (before < (uint32_t)kk && (uint32_t)kk <= before + tot) {
-                uint32_t acc = before;
-                int digit = 255 - 4 * t - 3;
+            if (lane == 31) s_wtot[warp] = inc;
+            s_hist[(pass + 1) & 1][t] = 0u;   // the other buffer is free: clear it for the next pass
+            __syncthreads();
+            uint32_t before = inc - cnt;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int bin = 255 - 4 * t - q;
-                    const uint32_t hq = s_hist[c][bin];
-                    if (acc + hq >= (uint32_t)kk) {
-                        digit = bin;
-                        break;
-                    }
-                    acc += hq;
-                }
-                s_sel[c][0] = digit;
-                s_sel[c][1] = kk - (int)acc;
+            for (int w = 0; w < kWarps; ++w)
+                if (w < warp) before += s_wtot[w];
+            if (before < (uint32_t)kk && (uint32_t)kk <= before + cnt) {
+                s_sel[0] = 255 - t;
+                s_sel[1] = kk - (int)before;
             }
-        }
-        __syncthreads();
-        if (active) {
-            prefix |= (uint32_t)s_sel[c][0] << shift;
+            __syncthreads();
+            prefix |= (uint32_t)s_sel[0] << shift;
             pmask |= 0xFFu << shift;
-            kk = s_sel[c][1];
+            kk = s_sel[1];
         }
-    }
-    const uint32_t tau = prefix;   // the top_k-th largest key; kk entries equal to tau are taken
+        const uint32_t tau = prefix;   // kk entries equal to tau are taken, lowest indices first
 
-    // ---- membership: keys above tau, and the first kk ties in index order ----
-#pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ((valid >> j) & 1u) && key[j] == tau);
-        if (lane == 0) s_bal[c][j][wg] = bal;
-    }
-    __syncthreads();
-    uint32_t member = 0u;
-    if (active) {
-        const uint32_t lt_mask = (1u << lane) - 1u;
-        int ties_before = 0;
+        // ---- membership: keys above tau, and the first kk ties in index order ----
 #pragma unroll
         for (int j = 0; j < EPT; ++j) {
-            const uint32_t b0 = s_bal[c][j][0], b1 = s_bal[c][j][1];
-            if ((valid >> j) & 1u) {
-                if (key[j] > tau) {
-                    member |= 1u << j;
-                } else if (key[j] == tau) {
-                    const int rank = ties_before + (wg ? __popc(b0) : 0) + __popc((wg ? b1 : b0) & lt_mask);
-                    if (rank < kk) member |= 1u << j;
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ((valid >> j) & 1u) && key[j] == tau);
+            if (lane == 0) s_bal[j][warp] = bal;
+        }
+        __syncthreads();
+        uint32_t member = 0u;
+        int nmine = 0;
+        {
+            const uint32_t lt_mask = (1u << lane) - 1u;
+            int ties_before = 0;
+#pragma unroll
+            for (int j = 0; j < EPT; ++j) {
+                int row_before = 0, row_total = 0;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    const int n = __popc(s_bal[j][w]);
+                    if (w < warp) row_before += n;
+                    row_total += n;
                 }
+                if ((valid >> j) & 1u) {
+                    bool take = key[j] > tau;
+                    if (key[j] == tau)
+                        take = ties_before + row_before + __popc(s_bal[j][warp] & lt_mask) < kk;
+                    if (take) {
+                        member |= 1u << j;
+                        ++nmine;
+                    }
+                }
+                ties_before += row_total;
             }
-            ties_before += __popc(b0) + __popc(b1);
         }
-    }
-
-    // ---- Gumbel-max draw over the members ---------------------------------
-    float best = -INFINITY;
-    int best_i = 0x7FFFFFFF;
-    if (active) {
-        const uint32_t k0 = (uint32_t)(seed & 0xFFFFFFFFull), k1 = (uint32_t)(seed >> 32);
+        // compact the kept indices (top_k of them) into s_list
+        int total = 0;
+        int slot = block_exclusive_scan(nmine, s_scan, total);
 #pragma unroll
-        for (int j = 0; j < EPT; ++j) {
-            if ((member >> j) & 1u) {
-                const int i = t + kGroup * j;
-                const uint4 r = philox4x32_10(make_uint4((uint32_t)i >> 2, (uint32_t)c, (uint32_t)step, (uint32_t)b),
-                                              k0, k1);
-                const uint32_t w = (i & 3) == 0 ? r.x : (i & 3) == 1 ? r.y : (i & 3) == 2 ? r.z : r.w;
-                const float u = (float)(2u * (w >> 9) + 1u) * 0x1p-24f;   // exact odd multiple of 2^-24
-                const float g = -logf(-logf(u));
-                const float s = key_value(key[j]) + g;
-                if (better(s, i, best, best_i)) {
-                    best = s;
-                    best_i = i;
-                }
+        for (int j = 0; j < EPT; ++j)
+            if ((member >> j) & 1u) s_list[slot++] = t + kThreads * j;
+        __syncthreads();
+
+        // ---- Gumbel-max draw over the list -------------------------------------
+        const uint64_t seed = p.seeds[b];
+        const uint32_t k0 = (uint32_t)(seed & 0xFFFFFFFFull), k1 = (uint32_t)(seed >> 32);
+        float best = -INFINITY;
+        int best_i = 0x7FFFFFFF;
+        for (int r = t; r < total; r += kThreads) {
+            const int i = s_list[r];
+            const float x = __fdiv_rn(__ldg(row + i), p.temperature);   // same rounding as the key
+            const uint4 w4 = philox4x32_10(make_uint4((uint32_t)i >> 2, (uint32_t)c, (uint32_t)step, (uint32_t)b),
+                                           k0, k1);
+            const uint32_t w = (i & 3) == 0 ? w4.x : (i & 3) == 1 ? w4.y : (i & 3) == 2 ? w4.z : w4.w;
+            const float u = (float)(2u * (w >> 9) + 1u) * 0x1p-24f;   // exact odd multiple of 2^-24
+            const float s = x - logf(-logf(u));
+            if (better(s, i, best, best_i)) {
+                best = s;
+                best_i = i;
             }
         }
 #pragma unroll
@@ -210,76 +245,101 @@ __global__ void __launch_bounds__(kMaxCodebooks *kGroup) sample_kernel(const Sam
             }
         }
         if (lane == 0) {
-            s_rf[c][wg] = best;
-            s_ri[c][wg] = best_i;
+            s_rf[warp] = best;
+            s_ri[warp] = best_i;
         }
-    }
-    __syncthreads();
-    if (t == 0) {
-        int tok = p.pad_id;
-        if (active) {
-            tok = better(s_rf[c][1], s_ri[c][1], s_rf[c][0], s_ri[c][0]) ? s_ri[c][1] : s_ri[c][0];
-        }
-        p.tokens[(size_t)b * p.C + c] = tok;
-    }
-
-    // ---- optional softmax over the members --------------------------------
-    if (p.probs) {
-        float xm = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < EPT; ++j)
-            if ((member >> j) & 1u) xm = fmaxf(xm, key_value(key[j]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) xm = fmaxf(xm, __shfl_xor_sync(0xFFFFFFFFu, xm, o));
-        __syncthreads();   // s_rf is reused below
-        if (lane == 0) s_rf[c][wg] = xm;
         __syncthreads();
-        xm = fmaxf(s_rf[c][0], s_rf[c][1]);
-        float z = 0.f;
-        if (xm != -INFINITY) {
+        if (t == 0) {
+            float bs = s_rf[0];
+            int bi = s_ri[0];
+            for (int w = 1; w < kWarps; ++w)
+                if (better(s_rf[w], s_ri[w], bs, bi)) {
+                    bs = s_rf[w];
+                    bi = s_ri[w];
+                }
+            p.tokens[(size_t)b * p.C + c] = bi;
+        }
+
+        // ---- optional softmax over the kept set -------------------------------
+        if (prow) {
+            float xm = -INFINITY;
 #pragma unroll
             for (int j = 0; j < EPT; ++j)
-                if ((member >> j) & 1u) z += expf(key_value(key[j]) - xm);
+                if ((member >> j) & 1u) xm = fmaxf(xm, key_value(key[j]));
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
-        }
-        __syncthreads();
-        if (lane == 0) s_rf[c][wg] = z;
-        __syncthreads();
-        z = s_rf[c][0] + s_rf[c][1];
-        float *prow = p.probs + ((size_t)b * p.C + c) * (size_t)p.V;
-        const float uniform = 1.0f / (float)p.top_k;
+            for (int o = 16; o > 0; o >>= 1) xm = fmaxf(xm, __shfl_xor_sync(0xFFFFFFFFu, xm, o));
+            __syncthreads();   // s_rf is reused
+            if (lane == 0) s_rf[warp] = xm;
+            __syncthreads();
+            xm = s_rf[0];
 #pragma unroll
-        for (int j = 0; j < EPT; ++j) {
-            const int i = t + kGroup * j;
-            if (i < p.V) {
-                float pr = 0.f;
-                if ((member >> j) & 1u) pr = (xm == -INFINITY) ? uniform : __fdiv_rn(expf(key_value(key[j]) - xm), z);
-                prow[i] = pr;
+            for (int w = 1; w < kWarps; ++w) xm = fmaxf(xm, s_rf[w]);
+            float z = 0.f;
+            if (xm != -INFINITY) {
+#pragma unroll
+                for (int j = 0; j < EPT; ++j)
+                    if ((member >> j) & 1u) z += expf(key_value(key[j]) - xm);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+            }
+            __syncthreads();
+            if (lane == 0) s_rf[warp] = z;
+            __syncthreads();
+            z = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) z += s_rf[w];
+            const float uniform = 1.0f / (float)p.top_k;
+#pragma unroll
+            for (int j = 0; j < EPT; ++j) {
+                const int i = t + kThreads * j;
+                if (i < p.V) {
+                    float pr = 0.f;
+                    if ((member >> j) & 1u)
+                        pr = (xm == -INFINITY) ? uniform : __fdiv_rn(expf(key_value(key[j]) - xm), z);
+                    prow[i] = pr;
+                }
             }
         }
     }
 
     if (p.flags & DR_SAMPLE_ADVANCE) {
-        __syncthreads();   // every group has read step[b]
-        if (threadIdx.x == 0) p.step[b] = step + 1;
+        // every thread of every codebook CTA of this row has read step[b] before it changes
+        if (gridDim.x > 1) cg::this_cluster().sync();
+        else __syncthreads();
+        if (blockIdx.x == 0 && t == 0) p.step[b] = step + 1;
     }
 }
 
 template <int EPT>
 cudaError_t launch_ept(const SampleParams &p, cudaStream_t stream) {
-    sample_kernel<EPT><<<(unsigned)p.B, (unsigned)(p.C * kGroup), 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.C, (unsigned)p.B, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = ((p.flags & DR_SAMPLE_ADVANCE) && p.C > 1) ? 1 : 0;
+    auto kern = sample_kernel<EPT>;
+    if (cfg.numAttrs && p.C > 8) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
 
 cudaError_t launch_sample(const SampleParams &p, cudaStream_t stream) {
-    const int ept = (p.V + kGroup - 1) / kGroup;
+    const int ept = (p.V + kThreads - 1) / kThreads;
+    if (ept <= 1) return launch_ept<1>(p, stream);
+    if (ept <= 2) return launch_ept<2>(p, stream);
     if (ept <= 4) return launch_ept<4>(p, stream);
-    if (ept <= 8) return launch_ept<8>(p, stream);
-    if (ept <= 17) return launch_ept<17>(p, stream);
-    return launch_ept<32>(p, stream);
+    if (ept <= 5) return launch_ept<5>(p, stream);
+    return launch_ept<8>(p, stream);
 }
 
 }  // namespace dr

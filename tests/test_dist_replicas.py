@@ -1,0 +1,73 @@
+"""Host-side logic of the N-GPU bench path, on CPU with two gloo ranks.
+
+The decode step shards by batch row with no collective on the data path: each
+rank runs its own replica (its own seeded batch), and only the timing is
+reduced -- the slowest rank's step time -- so the whole-job throughput is
+units of all ranks / max time.
+"""
+import os
+import socket
+
+import torch
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, results):
+    import sys
+
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import bench
+
+    ws, r, local = bench.dist_env()
+    assert (ws, r, local) == (world, rank, rank)
+    d = bench.init_dist(ws, "gloo")
+    local_ms = 10.0 + 5.0 * rank                    # rank 1 is the slow one
+    bench.barrier(d)
+    ms = bench.max_over_ranks(d, local_ms, torch.device("cpu"))
+    results[rank] = ms
+    d.destroy_process_group()
+
+
+def test_two_rank_max_over_ranks_gloo():
+    world = 2
+    port = _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    results = mgr.dict()
+    mp.start_processes(_worker, args=(world, port, results), nprocs=world, start_method="spawn", join=True)
+    assert dict(results) == {0: 15.0, 1: 15.0}
+
+
+def test_weak_scaling_value_counts_every_rank():
+    import numpy as np
+
+    import bench
+    from decode_attention_self_gb300 import workloads as W
+
+    w = W.make_workload(4)
+    sb = bench.step_bytes(w)
+    # per layer: valid K+V of every row, q and out, block-table entries; the step adds the sampler
+    L = w.seq_len.astype(np.int64)
+    expect_self = 4 * 16 * 64 * int(L.sum()) + 32 * 16 * 64 * (2 + 2) + 4 * int(((L + 15) // 16).sum())
+    assert sb["self"] == expect_self
+    assert sb["sampler"] == 32 * 9 * 1088 * 4 + 32 * 9 * 4
+    assert sb["step"] == 24 * (sb["self"] + sb["cross"] + sb["append"]) + sb["sampler"]
+
+
+def test_replicas_draw_distinct_batches():
+    # each rank's replica is seeded by its rank: different data, same shapes
+    from decode_attention_self_gb300 import workloads as W
+
+    w = W.make_workload(1)
+    a = W.make_step_inputs(w, 1000 * 0 + 0)[0]
+    b = W.make_step_inputs(w, 1000 * 1 + 0)[0]
+    assert a.shape == b.shape and not torch.equal(a, b)
