@@ -59,7 +59,48 @@ __device__ __forceinline__ void merge_state(float &m, float &l, float (&a)[N], f
     m = mm;
 }
 
-template <bool kPaged>
+// One lane group's online-softmax update with a 16-key tile: this lane holds
+// dims 8*sub..8*sub+7 of keys t+grp, t+grp+4, t+grp+8, t+grp+12.
+__device__ __forceinline__ void consume_tile(const uint4 (&kw)[4], const uint4 (&vw)[4], const float (&qf)[8], int t,
+                                             int grp, int key1, float &m, float &l, float (&acc)[8]) {
+    float sc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        float kf[8];
+        unpack8(kw[u], kf);
+        float d = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) d = fmaf(qf[j], kf[j], d);
+        d += __shfl_xor_sync(0xFFFFFFFFu, d, 1);
+        d += __shfl_xor_sync(0xFFFFFFFFu, d, 2);
+        d += __shfl_xor_sync(0xFFFFFFFFu, d, 4);
+        sc[u] = (t + grp + 4 * u < key1) ? d : -INFINITY;
+    }
+    const float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+    const float mn = fmaxf(m, mt);
+    if (mn == -INFINITY) return;   // this lane group had no valid key yet
+    const float corr = exp2f(m - mn);
+    l *= corr;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] *= corr;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float pu = exp2f(sc[u] - mn);
+        l += pu;
+        float vf[8];
+        unpack8(vw[u], vf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(pu, vf[j], acc[j]);
+    }
+    m = mn;
+}
+
+// kPipelined: each warp keeps the next tile's loads in flight while it
+// computes the current one (twice the bytes in flight per warp, at ~100
+// registers instead of 64).  Chosen when the whole grid is resident at once,
+// i.e. when occupancy is not what limits the bytes in flight.  Both variants
+// perform the same arithmetic in the same order.
+template <bool kPaged, bool kPipelined>
 __global__ void __launch_bounds__(kThreads) decode_attn_kernel(const AttnParams p) {
     __shared__ float s_wm[kWarps], s_wl[kWarps];
     __shared__ float s_wacc[kWarps][kD];
@@ -95,16 +136,15 @@ __global__ void __launch_bounds__(kThreads) decode_attn_kernel(const AttnParams 
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 
-    for (int t = key0 + warp * kTile; t < key1; t += kWarps * kTile) {
+    // Issue the 16-byte loads of tile t (zeros past key1 or for an unmapped block).
+    auto load_tile = [&](int t, uint4 (&kw)[4], uint4 (&vw)[4]) -> bool {
         const uint16_t *kt;
         const uint16_t *vt;
+        bool ok = true;
         if constexpr (kPaged) {
             const int blk = __ldg(p.table + (size_t)b * p.max_blocks + t / kTile);
-            if ((unsigned)blk >= (unsigned)p.num_blocks) {
-                if (lane == 0) flag_error(p.err, DR_ERRF_BLOCK_ID);
-                continue;   // warp-uniform: the whole tile is skipped
-            }
-            const size_t off = ((size_t)blk * p.H + h) * (size_t)(kTile * kD);
+            ok = (unsigned)blk < (unsigned)p.num_blocks;
+            const size_t off = ok ? ((size_t)blk * p.H + h) * (size_t)(kTile * kD) : 0;
             kt = p.k + off;
             vt = p.v + off;
         } else {
@@ -112,12 +152,10 @@ __global__ void __launch_bounds__(kThreads) decode_attn_kernel(const AttnParams 
             kt = p.k + off;
             vt = p.v + off;
         }
-
-        uint4 kw[4], vw[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int r = grp + 4 * u;
-            if (t + r < key1) {
+            if (ok && t + r < key1) {
                 kw[u] = ld_stream16(kt + r * kD + sub * 8);
                 vw[u] = ld_stream16(vt + r * kD + sub * 8);
             } else {
@@ -125,37 +163,32 @@ __global__ void __launch_bounds__(kThreads) decode_attn_kernel(const AttnParams 
                 vw[u] = make_uint4(0, 0, 0, 0);
             }
         }
+        return ok;
+    };
 
-        float sc[4];
+    if constexpr (kPipelined) {
+        uint4 kw[4], vw[4];
+        int t = key0 + warp * kTile;
+        bool ok = t < key1 ? load_tile(t, kw, vw) : true;
+        for (; t < key1; t += kWarps * kTile) {
+            uint4 nk[4] = {}, nv[4] = {};
+            const int tn = t + kWarps * kTile;
+            const bool nok = tn < key1 ? load_tile(tn, nk, nv) : true;
+            if (ok) consume_tile(kw, vw, qf, t, grp, key1, m, l, acc);
+            else if (lane == 0) flag_error(p.err, DR_ERRF_BLOCK_ID);   // warp-uniform: the tile is skipped
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float kf[8];
-            unpack8(kw[u], kf);
-            float d = 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) d = fmaf(qf[j], kf[j], d);
-            d += __shfl_xor_sync(0xFFFFFFFFu, d, 1);
-            d += __shfl_xor_sync(0xFFFFFFFFu, d, 2);
-            d += __shfl_xor_sync(0xFFFFFFFFu, d, 4);
-            sc[u] = (t + grp + 4 * u < key1) ? d : -INFINITY;
+            for (int u = 0; u < 4; ++u) {
+                kw[u] = nk[u];
+                vw[u] = nv[u];
+            }
+            ok = nok;
         }
-        const float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-        const float mn = fmaxf(m, mt);
-        if (mn == -INFINITY) continue;   // this lane group had no valid key yet
-        const float corr = exp2f(m - mn);
-        l *= corr;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] *= corr;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float pu = exp2f(sc[u] - mn);
-            l += pu;
-            float vf[8];
-            unpack8(vw[u], vf);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = fmaf(pu, vf[j], acc[j]);
+    } else {
+        for (int t = key0 + warp * kTile; t < key1; t += kWarps * kTile) {
+            uint4 kw[4], vw[4];
+            if (load_tile(t, kw, vw)) consume_tile(kw, vw, qf, t, grp, key1, m, l, acc);
+            else if (lane == 0) flag_error(p.err, DR_ERRF_BLOCK_ID);   // warp-uniform: the tile is skipped
         }
-        m = mn;
     }
 
     // Lanes sub, sub+8, sub+16, sub+24 hold the same dims for different keys.
@@ -238,9 +271,8 @@ __global__ void __launch_bounds__(kThreads) decode_attn_kernel(const AttnParams 
     cluster.sync();   // keep every CTA's shared memory alive until rank 0 has read it
 }
 
-}  // namespace
-
-cudaError_t launch_decode_attn(const AttnParams &p, bool paged, int splits, cudaStream_t stream) {
+template <bool kPaged, bool kPipelined>
+cudaError_t launch_variant(const AttnParams &p, int splits, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)splits, (unsigned)p.H, (unsigned)p.B);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -253,14 +285,24 @@ cudaError_t launch_decode_attn(const AttnParams &p, bool paged, int splits, cuda
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = splits > 1 ? 1 : 0;
-    if (paged) {
-        auto kern = decode_attn_kernel<true>;
-        if (splits > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        return cudaLaunchKernelEx(&cfg, kern, p);
+    auto kern = decode_attn_kernel<kPaged, kPipelined>;
+    if (splits > 8) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
     }
-    auto kern = decode_attn_kernel<false>;
-    if (splits > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// CTAs of the pipelined kernel that fit on one SM at once (up to 112 registers x 128 threads).
+constexpr int kPipelinedCtasPerSm = 4;
+
+}  // namespace
+
+cudaError_t launch_decode_attn(const AttnParams &p, bool paged, int splits, cudaStream_t stream) {
+    const long long ctas = (long long)splits * p.H * p.B;
+    const bool pipelined = ctas <= (long long)kPipelinedCtasPerSm * current_device_sms();
+    if (paged) return pipelined ? launch_variant<true, true>(p, splits, stream) : launch_variant<true, false>(p, splits, stream);
+    return pipelined ? launch_variant<false, true>(p, splits, stream) : launch_variant<false, false>(p, splits, stream);
 }
 
 }  // namespace dr

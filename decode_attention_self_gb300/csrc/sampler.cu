@@ -12,8 +12,8 @@
 //      registers), divides by T with IEEE round-to-nearest and maps each float
 //      to an order-preserving uint32 key;
 //   2. finds the top_k-th largest key tau by a 4-pass, 8-bit radix select:
-//      shared-memory histograms filled with warp-aggregated atomics (lanes
-//      holding the same digit add once), scanned in descending digit order;
+//      double-buffered shared-memory histograms (shared atomics), scanned in
+//      descending digit order, three barriers per pass;
 //   3. keeps every key > tau plus the lowest-index entries equal to tau (their
 //      rank in index order comes from warp ballots), so ties go to the lower
 //      index exactly, and compacts the kept indices into a shared list;
@@ -144,10 +144,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) 
             uint32_t *hist = s_hist[pass & 1];
 #pragma unroll
             for (int j = 0; j < EPT; ++j) {
-                const bool in = ((valid >> j) & 1u) && (key[j] & pmask) == prefix;
-                const uint32_t digit = in ? (key[j] >> shift) & 255u : 0x100u;
-                const uint32_t peers = __match_any_sync(0xFFFFFFFFu, digit);
-                if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+                if (((valid >> j) & 1u) && (key[j] & pmask) == prefix) atomicAdd(&hist[(key[j] >> shift) & 255u], 1u);
             }
             __syncthreads();
             // thread t owns digit 255 - t: an inclusive scan over t walks digits downward

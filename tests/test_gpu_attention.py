@@ -268,3 +268,24 @@ def test_calls_capture_into_a_cuda_graph(api, cuda_device):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out_e, out_g)
+
+
+def test_row_result_independent_of_batch_and_kernel_variant(api, cuda_device):
+    # A row alone (B=1: the whole grid is resident, the pipelined variant runs) and the same row inside a
+    # batch of 96 (the streaming variant runs) share the split plan (8 CTAs per row for a 4096-key bound),
+    # and the two variants do the same arithmetic in the same order: the outputs must be bit-identical.
+    from decode_attention_self_gb300 import api as _api
+    dev = cuda_device
+    lens = [4000] + [int(x) for x in np.random.default_rng(13).integers(1000, 4096, size=95)]
+    w, cache, q = ragged_case("paged", lens, 4096, seed=13)
+    assert api.dr_plan_splits(1, 16, 4096, 152) == api.dr_plan_splits(96, 16, 4096, 152) == 8
+    kv = to_dev(cache, dev)
+    seq = torch.from_numpy(w.seq_len).to(dev)
+    big = torch.empty((w.B, 16, D), dtype=torch.float32, device=dev)
+    api.dr_decode_self_attn(q.to(dev), kv, seq, big, max_seq_len_hint=4096)
+    one_kv = _api.KVCache(kv.k, kv.v, kv.block_table[:1].contiguous())
+    one = torch.empty((1, 16, D), dtype=torch.float32, device=dev)
+    api.dr_decode_self_attn(q[:1].contiguous().to(dev), one_kv, seq[:1].contiguous(), one, max_seq_len_hint=4096)
+    torch.cuda.synchronize()
+    assert torch.equal(one[0], big[0])
+    assert_attn_close(big[:2], oracle_self(w, cache, q, default_scale(D))[:2])
