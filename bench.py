@@ -174,10 +174,13 @@ def committed_traffic(kernel_key: str):
 # the step on the GPU
 # ---------------------------------------------------------------------------
 class DeviceStep:
-    def __init__(self, w: W.Workload, dev, rank: int):
+    """One decode step on the GPU: per layer one fused dr_decode_layer launch (append + self + cross), or with
+    fused=False the three separate calls; then dr_sample_topk_delayed once."""
+
+    def __init__(self, w: W.Workload, dev, rank: int, fused: bool = True):
         from decode_attention_self_gb300 import api
 
-        self.api, self.w, self.dev = api, w, dev
+        self.api, self.w, self.dev, self.fused = api, w, dev, fused
         self.layers = []
         for l in range(w.layers):
             c = W.make_self_cache(w, 1000 * rank + l, device=dev)
@@ -198,25 +201,37 @@ class DeviceStep:
         self.hint = int(w.seq_len.max())
 
     def launches_per_step(self) -> int:
-        return 3 * self.w.layers + 1
+        return (1 if self.fused else 3) * self.w.layers + 1
 
-    def run(self, ev_self=None, ev_samp=None):
-        api, w = self.api, self.w
-        for l, L in enumerate(self.layers):
+    def run_layer(self, l):
+        api, L = self.api, self.layers[l]
+        if self.fused:
+            api.dr_decode_layer(L["q"], L["kv"], L["kn"], L["vn"], self.seq, L["qx"], L["kx"], L["vx"], self.enc,
+                                self.out_s[l], self.out_x[l], max_seq_len_hint=self.hint, err_flag=self.err)
+        else:
             api.dr_kv_append(L["kv"], L["kn"], L["vn"], self.pos, err_flag=self.err)
-            if ev_self is not None:
-                ev_self[l][0].record()
             api.dr_decode_self_attn(L["q"], L["kv"], self.seq, self.out_s[l], max_seq_len_hint=self.hint,
                                     err_flag=self.err)
-            if ev_self is not None:
-                ev_self[l][1].record()
             api.dr_decode_cross_attn(L["qx"], L["kx"], L["vx"], self.enc, self.out_x[l], err_flag=self.err)
-        if ev_samp is not None:
-            ev_samp[0].record()
-        api.dr_sample_topk_delayed(self.logits, w.temperature, w.top_k, self.seeds, self.step, w.pad_id,
-                                   self.tokens, V=w.V)
-        if ev_samp is not None:
-            ev_samp[1].record()
+
+    def run_dominant(self):
+        """The dominant kernel's launches of one step: the fused layer launches, or the self-attention calls."""
+        for l, L in enumerate(self.layers):
+            if self.fused:
+                self.run_layer(l)
+            else:
+                self.api.dr_decode_self_attn(L["q"], L["kv"], self.seq, self.out_s[l], max_seq_len_hint=self.hint,
+                                             err_flag=self.err)
+
+    def run_sampler_only(self):
+        w = self.w
+        self.api.dr_sample_topk_delayed(self.logits, w.temperature, w.top_k, self.seeds, self.step, w.pad_id,
+                                        self.tokens, V=w.V)
+
+    def run(self):
+        for l in range(self.w.layers):
+            self.run_layer(l)
+        self.run_sampler_only()
 
 
 class HostStep:
@@ -335,6 +350,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps one by one instead of a CUDA graph")
+    ap.add_argument("--unfused", action="store_true",
+                    help="three launches per layer (append, self, cross) instead of one dr_decode_layer launch")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     w = W.make_workload(args.workload)
@@ -367,7 +384,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist = init_dist(ws, "nccl")
-    ds = DeviceStep(w, dev, rank)
+    ds = DeviceStep(w, dev, rank, fused=not args.unfused)
     torch.cuda.synchronize()
 
     for _ in range(max(3, args.warmup)):
@@ -375,60 +392,73 @@ def main():
     torch.cuda.synchronize()
     assert int(ds.err.item()) == 0, "device error flag set during warm-up"
 
-    # The timed region is K decode steps.  By default they are captured as one CUDA graph
-    # (the page's own way of removing launch overhead), with event nodes around every
-    # self-attention and sampler launch; --eager launches them one by one instead.
+    # The timed region is K decode steps, captured as one CUDA graph (the page's own way of
+    # removing launch overhead) with no event nodes inside it; --eager launches them one by one.
+    # The dominant kernel's average launch duration is then timed the same way on its own:
+    # a graph of its K x layers launches of the timed steps, back to back (same arguments),
+    # bracketed by events; likewise the sampler's K launches.
     K = args.steps
     mode = "eager" if args.eager else "cuda_graph"
-    graph = None
-    if not args.eager:
-        try:
-            mk = lambda: torch.cuda.Event(enable_timing=True, external=True)
-            ev_self = [[(mk(), mk()) for _ in range(w.layers)] for _ in range(K)]
-            ev_samp = [(mk(), mk()) for _ in range(K)]
-            graph = torch.cuda.CUDAGraph()
-            cs = torch.cuda.Stream()
-            cs.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.graph(graph, stream=cs):
-                for i in range(K):
-                    ds.run(ev_self[i], ev_samp[i])
-            torch.cuda.current_stream().wait_stream(cs)
-            graph.replay()                                 # untimed: instantiation and first-touch costs
-            torch.cuda.synchronize()
-        except TypeError:                                  # a torch without external (graph-node) events
-            graph, mode = None, "eager"
-    if graph is None:
-        mk = lambda: torch.cuda.Event(enable_timing=True)
-        ev_self = [[(mk(), mk()) for _ in range(w.layers)] for _ in range(K)]
-        ev_samp = [(mk(), mk()) for _ in range(K)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(dist)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t0.record()
-        if graph is not None:
-            graph.replay()
-        else:
-            for i in range(K):
-                ds.run(ev_self[i], ev_samp[i])
-        t1.record()
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream()
+        cs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cs):
+            fn()
+        torch.cuda.current_stream().wait_stream(cs)
+        g.replay()                                         # untimed: instantiation and first-touch costs
         torch.cuda.synchronize()
+        return g
+
+    def steps():
+        for _ in range(K):
+            ds.run()
+
+    def self_only():
+        for _ in range(K):
+            ds.run_dominant()
+
+    def sampler_only():
+        for _ in range(K):
+            ds.run_sampler_only()
+
+    regions = {"step": steps, "self": self_only, "sampler": sampler_only}
+    graphs = {k: capture(f) for k, f in regions.items()} if not args.eager else None
+
+    def timed(name):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0.record()
+        if graphs is not None:
+            graphs[name].replay()
+        else:
+            regions[name]()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    with ClockSampler(local) as clk:
+        step_total_ms = timed("step")
+        self_total_ms = timed("self")
+        samp_total_ms = timed("sampler")
     barrier(dist)
-    ms = t0.elapsed_time(t1) / K
-    ms = max_over_ranks(dist, ms, dev)
-    self_ms = [a.elapsed_time(b) for row in ev_self for a, b in row]
-    samp_ms = [a.elapsed_time(b) for a, b in ev_samp]
-    self_avg_ms = sum(self_ms) / len(self_ms)
+    ms = max_over_ranks(dist, step_total_ms / K, dev)
+    self_avg_ms = self_total_ms / (K * w.layers)
+    samp_avg_ms = samp_total_ms / K
     value = sb["step"] * ws / (ms * 1e-3) / 1e9
 
     peaks, peak_kind = measured_peaks()
-    achieved = sb["self"] / (self_avg_ms * 1e-3) / 1e9
-    traffic = committed_traffic(f"decode_attn_kernel workload {w.index}")
+    dom_bytes = sb["self"] + sb["cross"] + sb["append"] if ds.fused else sb["self"]
+    achieved = dom_bytes / (self_avg_ms * 1e-3) / 1e9
+    kname = "decode_attn_kernel<fused>" if ds.fused else "decode_attn_kernel"
+    traffic = committed_traffic(f"{kname} workload {w.index}")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
-                "kernel": "decode_attn_kernel (dr_decode_self_attn)", "peak_kind": peak_kind,
-                "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS, "algorithmic_bytes_per_launch": sb["self"],
-                "avg_launch_us": self_avg_ms * 1e3}
+                "kernel": kname + (" (dr_decode_layer: append + self + cross)" if ds.fused else " (dr_decode_self_attn)"),
+                "peak_kind": peak_kind, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_us": self_avg_ms * 1e3}
 
     e2e = None
     if not args.no_e2e:
@@ -459,10 +489,13 @@ def main():
                 "dtype": "bf16", "data": "synthetic",
                 "config": {**config, "l2": "inputs larger than L2 (%.1f GB per step vs 129 MB)" % (sb["step"] / 1e9)
                            if sb["step"] > L2_BYTES else "inputs smaller than L2: warm-L2 figure"},
-                "us_per_step": ms * 1e3, "self_attn_us": self_avg_ms * 1e3,
-                "sampler_us": sum(samp_ms) / len(samp_ms) * 1e3,
+                "us_per_step": ms * 1e3, "layer_us" if ds.fused else "self_attn_us": self_avg_ms * 1e3,
+                "sampler_us": samp_avg_ms * 1e3,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": ds.launches_per_step() * K, "launch_mode": mode, "clocks": clk.summary()}
+                "gpu_launches": ds.launches_per_step() * K, "launch_mode": mode,
+                "kernel_timing": "dominant kernel and sampler: K x layers (K) launches of the timed steps, "
+                                 "back to back in their own graph, events around it",
+                "clocks": clk.summary()}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

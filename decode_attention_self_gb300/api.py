@@ -41,12 +41,15 @@ _vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _lib.dr_kv_append.argtypes = [ctypes.POINTER(dr_kv_cache), _vp, _vp, _vp, _i, _i, _i, _vp, _vp]
 _lib.dr_decode_self_attn.argtypes = [_vp, ctypes.POINTER(dr_kv_cache), _vp, _i, _i, _i, _i, _f, _vp, _i, _vp, _vp]
 _lib.dr_decode_cross_attn.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _i, _vp, _vp]
+_lib.dr_decode_layer.argtypes = [_vp, ctypes.POINTER(dr_kv_cache), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
+                                 _i, _f, _vp, _vp, _i, _vp, _vp]
 _lib.dr_sample_topk_delayed.argtypes = [_vp, _i, _i, _i, _i, _f, _i, _vp, _vp, ctypes.c_int32, _vp, _vp, _i, _vp]
 _lib.dr_plan_splits.argtypes = [_i, _i, _i, _i]
 _lib.dr_plan_splits.restype = _i
 _lib.dr_status_string.argtypes = [_i]
 _lib.dr_status_string.restype = ctypes.c_char_p
-for _fn in ("dr_kv_append", "dr_decode_self_attn", "dr_decode_cross_attn", "dr_sample_topk_delayed"):
+for _fn in ("dr_kv_append", "dr_decode_self_attn", "dr_decode_cross_attn", "dr_decode_layer",
+            "dr_sample_topk_delayed"):
     getattr(_lib, _fn).restype = _i
 
 
@@ -159,6 +162,26 @@ def dr_decode_cross_attn(q: torch.Tensor, k_enc: torch.Tensor, v_enc: torch.Tens
                                      B, H, D, Lc_max, float(scale), _ptr(out, None, "out"), od,
                                      _ptr(err_flag, torch.int32, "err_flag"), _stream(stream)))
     return out
+
+
+def dr_decode_layer(q: torch.Tensor, cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, seq_len: torch.Tensor,
+                    q_cross: torch.Tensor, k_enc: torch.Tensor, v_enc: torch.Tensor, enc_len: torch.Tensor,
+                    out: torch.Tensor, out_cross: torch.Tensor, max_seq_len_hint: int = 0, scale: float = 0.0,
+                    err_flag: torch.Tensor | None = None, stream=None) -> None:
+    """One launch: append k_new, v_new at seq_len-1, self-attention over seq_len keys, cross-attention."""
+    B, H, D = q.shape
+    if out_cross.dtype != out.dtype:
+        raise ValueError("out and out_cross must have the same dtype")
+    c = cache.as_c()
+    od = DR_F32 if out.dtype == torch.float32 else DR_BF16
+    _check("dr_decode_layer",
+           _lib.dr_decode_layer(_ptr(q, torch.bfloat16, "q"), ctypes.byref(c), _ptr(k_new, torch.bfloat16, "k_new"),
+                                _ptr(v_new, torch.bfloat16, "v_new"), _ptr(seq_len, torch.int32, "seq_len"),
+                                _ptr(q_cross, torch.bfloat16, "q_cross"), _ptr(k_enc, torch.bfloat16, "k_enc"),
+                                _ptr(v_enc, torch.bfloat16, "v_enc"), _ptr(enc_len, torch.int32, "enc_len"),
+                                k_enc.shape[2], B, H, D, int(max_seq_len_hint), float(scale), _ptr(out, None, "out"),
+                                _ptr(out_cross, None, "out_cross"), od, _ptr(err_flag, torch.int32, "err_flag"),
+                                _stream(stream)))
 
 
 def dr_sample_topk_delayed(logits: torch.Tensor, temperature: float, top_k: int, seeds: torch.Tensor,

@@ -100,8 +100,8 @@ __device__ __forceinline__ void consume_tile(const uint4 (&kw)[4], const uint4 (
 // registers instead of 64).  Chosen when the whole grid is resident at once,
 // i.e. when occupancy is not what limits the bytes in flight.  Both variants
 // perform the same arithmetic in the same order.
-template <bool kPaged, bool kPipelined>
-__global__ void __launch_bounds__(kThreads) decode_attn_kernel(const AttnParams p) {
+template <bool kPaged, bool kPipelined, bool kFused>
+__global__ void __launch_bounds__(kThreads, kPipelined ? 4 : (kFused ? 6 : 8)) decode_attn_kernel(const AttnParams p) {
     __shared__ float s_wm[kWarps], s_wl[kWarps];
     __shared__ float s_wacc[kWarps][kD];
     __shared__ SoftmaxPartial s_part;
@@ -109,16 +109,30 @@ __global__ void __launch_bounds__(kThreads) decode_attn_kernel(const AttnParams 
     const int split = blockIdx.x;
     const int nsplit = gridDim.x;
     const int h = blockIdx.y;
-    const int b = blockIdx.z;
+    // Fused launches carry B self rows then B cross rows along z.
+    const bool cross = kFused && p.xq != nullptr && (int)blockIdx.z >= p.B;
+    const int b = cross ? (int)blockIdx.z - p.B : (int)blockIdx.z;
+    const bool paged = kPaged && !cross;
+    const uint16_t *qsrc = cross ? p.xq : p.q;
+    const uint16_t *kcache = cross ? p.xk : p.k;
+    const uint16_t *vcache = cross ? p.xv : p.v;
+    const int cap = cross ? p.xcap : p.cap;
+    void *outp = cross ? p.xout : p.out;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int grp = lane >> 3;   // which key of each group of 4
     const int sub = lane & 7;    // which 8 dims
 
-    int L = __ldg(p.lens + b);
-    if (L < 1 || L > p.cap) {
-        if (split == 0 && h == 0 && threadIdx.x == 0) flag_error(p.err, DR_ERRF_SEQ_LEN);
-        L = L < 0 ? 0 : (L > p.cap ? p.cap : L);
+    int L = __ldg((cross ? p.xlens : p.lens) + b);
+    // Fused append: this step's key goes to slot L-1 (only for a valid length).
+    int newpos = -1;
+    if (kFused && !cross && p.k_new != nullptr && L >= 1 && L <= cap) newpos = L - 1;
+    if (L < 1 || L > cap) {
+        if (split == 0 && h == 0 && threadIdx.x == 0) {
+            flag_error(p.err, DR_ERRF_SEQ_LEN);
+            if (kFused && !cross && p.k_new != nullptr) flag_error(p.err, DR_ERRF_POS);
+        }
+        L = L < 0 ? 0 : (L > cap ? cap : L);
     }
     const int ntiles = (L + kTile - 1) / kTile;
     const int per = (ntiles + nsplit - 1) / nsplit;
@@ -127,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) decode_attn_kernel(const AttnParams 
 
     const size_t row = (size_t)b * p.H + h;
     float qf[8];
-    unpack8(ld_ro16(p.q + row * kD + sub * 8), qf);
+    unpack8(ld_ro16(qsrc + row * kD + sub * 8), qf);
 #pragma unroll
     for (int j = 0; j < 8; ++j) qf[j] *= p.qscale;
 
@@ -137,32 +151,42 @@ __global__ void __launch_bounds__(kThreads) decode_attn_kernel(const AttnParams 
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 
     // Issue the 16-byte loads of tile t (zeros past key1 or for an unmapped block).
+    // Fused: the key at newpos is this step's k_new/v_new, taken from the inputs
+    // and stored into its cache slot by the same lanes.
     auto load_tile = [&](int t, uint4 (&kw)[4], uint4 (&vw)[4]) -> bool {
         const uint16_t *kt;
         const uint16_t *vt;
         bool ok = true;
-        if constexpr (kPaged) {
+        if (paged) {
             const int blk = __ldg(p.table + (size_t)b * p.max_blocks + t / kTile);
             ok = (unsigned)blk < (unsigned)p.num_blocks;
             const size_t off = ok ? ((size_t)blk * p.H + h) * (size_t)(kTile * kD) : 0;
-            kt = p.k + off;
-            vt = p.v + off;
+            kt = kcache + off;
+            vt = vcache + off;
         } else {
-            const size_t off = (row * (size_t)p.cap + (size_t)t) * kD;
-            kt = p.k + off;
-            vt = p.v + off;
+            const size_t off = (row * (size_t)cap + (size_t)t) * kD;
+            kt = kcache + off;
+            vt = vcache + off;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int r = grp + 4 * u;
             if (ok && t + r < key1) {
-                kw[u] = ld_stream16(kt + r * kD + sub * 8);
-                vw[u] = ld_stream16(vt + r * kD + sub * 8);
+                if (kFused && t + r == newpos) {
+                    kw[u] = ld_ro16(p.k_new + row * kD + sub * 8);
+                    vw[u] = ld_ro16(p.v_new + row * kD + sub * 8);
+                    *reinterpret_cast<uint4 *>(const_cast<uint16_t *>(kt) + r * kD + sub * 8) = kw[u];
+                    *reinterpret_cast<uint4 *>(const_cast<uint16_t *>(vt) + r * kD + sub * 8) = vw[u];
+                } else {
+                    kw[u] = ld_stream16(kt + r * kD + sub * 8);
+                    vw[u] = ld_stream16(vt + r * kD + sub * 8);
+                }
             } else {
                 kw[u] = make_uint4(0, 0, 0, 0);
                 vw[u] = make_uint4(0, 0, 0, 0);
             }
         }
+        if (kFused && !ok && t <= newpos && newpos < t + kTile && lane == 0) flag_error(p.err, DR_ERRF_POS);
         return ok;
     };
 
@@ -231,8 +255,8 @@ __global__ void __launch_bounds__(kThreads) decode_attn_kernel(const AttnParams 
         }
     }
 
-    float *out_f = reinterpret_cast<float *>(p.out) + row * kD;
-    uint16_t *out_h = reinterpret_cast<uint16_t *>(p.out) + row * kD;
+    float *out_f = reinterpret_cast<float *>(outp) + row * kD;
+    uint16_t *out_h = reinterpret_cast<uint16_t *>(outp) + row * kD;
 
     if (nsplit == 1) {
         __syncthreads();
@@ -271,10 +295,11 @@ __global__ void __launch_bounds__(kThreads) decode_attn_kernel(const AttnParams 
     cluster.sync();   // keep every CTA's shared memory alive until rank 0 has read it
 }
 
-template <bool kPaged, bool kPipelined>
+template <bool kPaged, bool kPipelined, bool kFused>
 cudaError_t launch_variant(const AttnParams &p, int splits, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)splits, (unsigned)p.H, (unsigned)p.B);
+    const unsigned zrows = (unsigned)p.B * ((kFused && p.xq) ? 2u : 1u);
+    cfg.gridDim = dim3((unsigned)splits, (unsigned)p.H, zrows);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -285,7 +310,7 @@ cudaError_t launch_variant(const AttnParams &p, int splits, cudaStream_t stream)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = splits > 1 ? 1 : 0;
-    auto kern = decode_attn_kernel<kPaged, kPipelined>;
+    auto kern = decode_attn_kernel<kPaged, kPipelined, kFused>;
     if (splits > 8) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
@@ -296,13 +321,22 @@ cudaError_t launch_variant(const AttnParams &p, int splits, cudaStream_t stream)
 // CTAs of the pipelined kernel that fit on one SM at once (up to 112 registers x 128 threads).
 constexpr int kPipelinedCtasPerSm = 4;
 
+template <bool kFused>
+cudaError_t launch_layout(const AttnParams &p, bool paged, int splits, cudaStream_t stream) {
+    const long long ctas = (long long)splits * p.H * p.B * ((kFused && p.xq) ? 2 : 1);
+    const bool pipelined = ctas <= (long long)kPipelinedCtasPerSm * current_device_sms();
+    if (paged)
+        return pipelined ? launch_variant<true, true, kFused>(p, splits, stream)
+                         : launch_variant<true, false, kFused>(p, splits, stream);
+    return pipelined ? launch_variant<false, true, kFused>(p, splits, stream)
+                     : launch_variant<false, false, kFused>(p, splits, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_decode_attn(const AttnParams &p, bool paged, int splits, cudaStream_t stream) {
-    const long long ctas = (long long)splits * p.H * p.B;
-    const bool pipelined = ctas <= (long long)kPipelinedCtasPerSm * current_device_sms();
-    if (paged) return pipelined ? launch_variant<true, true>(p, splits, stream) : launch_variant<true, false>(p, splits, stream);
-    return pipelined ? launch_variant<false, true>(p, splits, stream) : launch_variant<false, false>(p, splits, stream);
+    const bool fused = p.k_new != nullptr || p.xq != nullptr;
+    return fused ? launch_layout<true>(p, paged, splits, stream) : launch_layout<false>(p, paged, splits, stream);
 }
 
 }  // namespace dr

@@ -67,16 +67,10 @@ float softmax_scale_log2(float scale, int D) {
     return s * 1.4426950408889634f;   // log2(e): the kernel works in base 2
 }
 
-dr_status attention(const void *q, const void *k, const void *v, const int32_t *lens, const int32_t *table,
-                    bool paged, int B, int H, int cap, int max_blocks, int num_blocks, int hint, float scale,
-                    void *out, dr_dtype out_dtype, int32_t *err_flag, void *stream) {
-    if (!q || !lens || !out || !aligned16(q)) return DR_ERR_INVALID_ARG;
-    if (out_dtype != DR_BF16 && out_dtype != DR_F32) return DR_ERR_INVALID_ARG;
-    if (!(scale == scale) || isinf(scale)) return DR_ERR_INVALID_ARG;
-    const int bound = (hint > 0 && hint < cap) ? hint : cap;
-    const int sms = dr::current_device_sms();
-    if (sms <= 0) return DR_ERR_CUDA;
-    dr::AttnParams p;
+void fill_self(dr::AttnParams &p, const void *q, const void *k, const void *v, const int32_t *lens,
+               const int32_t *table, int B, int H, int cap, int max_blocks, int num_blocks, float scale, void *out,
+               dr_dtype out_dtype, int32_t *err_flag) {
+    p = dr::AttnParams{};
     p.q = static_cast<const uint16_t *>(q);
     p.k = static_cast<const uint16_t *>(k);
     p.v = static_cast<const uint16_t *>(v);
@@ -91,7 +85,20 @@ dr_status attention(const void *q, const void *k, const void *v, const int32_t *
     p.out = out;
     p.out_f32 = out_dtype == DR_F32;
     p.err = err_flag;
-    const int splits = dr_plan_splits(B, H, bound, sms);
+}
+
+dr_status check_attn_args(const void *q, const int32_t *lens, void *out, dr_dtype out_dtype, float scale) {
+    if (!q || !lens || !out || !aligned16(q)) return DR_ERR_INVALID_ARG;
+    if (out_dtype != DR_BF16 && out_dtype != DR_F32) return DR_ERR_INVALID_ARG;
+    if (!(scale == scale) || isinf(scale)) return DR_ERR_INVALID_ARG;
+    return DR_OK;
+}
+
+dr_status launch(const dr::AttnParams &p, bool paged, int hint, void *stream) {
+    const int bound = (hint > 0 && hint < p.cap) ? hint : p.cap;
+    const int sms = dr::current_device_sms();
+    if (sms <= 0) return DR_ERR_CUDA;
+    const int splits = dr_plan_splits(p.B, p.H, bound, sms);
     return from_cuda(dr::launch_decode_attn(p, paged, splits, static_cast<cudaStream_t>(stream)));
 }
 
@@ -147,10 +154,13 @@ dr_status dr_decode_self_attn(const void *q, const dr_kv_cache *cache, const int
     int cap = 0;
     st = check_cache(cache, &cap);
     if (st != DR_OK) return st;
+    st = check_attn_args(q, seq_len, out, out_dtype, scale);
+    if (st != DR_OK) return st;
     const bool paged = cache->layout == DR_KV_PAGED;
-    return attention(q, cache->k, cache->v, seq_len, paged ? cache->block_table : nullptr, paged, B, H, cap,
-                     paged ? cache->max_blocks_per_seq : 0, paged ? cache->num_blocks : 0, max_seq_len_hint, scale,
-                     out, out_dtype, err_flag, stream);
+    dr::AttnParams p;
+    fill_self(p, q, cache->k, cache->v, seq_len, paged ? cache->block_table : nullptr, B, H, cap,
+              paged ? cache->max_blocks_per_seq : 0, paged ? cache->num_blocks : 0, scale, out, out_dtype, err_flag);
+    return launch(p, paged, max_seq_len_hint, stream);
 }
 
 dr_status dr_decode_cross_attn(const void *q, const void *k_enc, const void *v_enc, const int32_t *enc_len, int B,
@@ -159,8 +169,41 @@ dr_status dr_decode_cross_attn(const void *q, const void *k_enc, const void *v_e
     dr_status st = check_dims(B, H, D);
     if (st != DR_OK) return st;
     if (!k_enc || !v_enc || Lc_max < 1 || !aligned16(k_enc) || !aligned16(v_enc)) return DR_ERR_INVALID_ARG;
-    return attention(q, k_enc, v_enc, enc_len, nullptr, false, B, H, Lc_max, 0, 0, Lc_max, scale, out, out_dtype,
-                     err_flag, stream);
+    st = check_attn_args(q, enc_len, out, out_dtype, scale);
+    if (st != DR_OK) return st;
+    dr::AttnParams p;
+    fill_self(p, q, k_enc, v_enc, enc_len, nullptr, B, H, Lc_max, 0, 0, scale, out, out_dtype, err_flag);
+    return launch(p, false, Lc_max, stream);
+}
+
+dr_status dr_decode_layer(const void *q, const dr_kv_cache *cache, const void *k_new, const void *v_new,
+                          const int32_t *seq_len, const void *q_cross, const void *k_enc, const void *v_enc,
+                          const int32_t *enc_len, int Lc_max, int B, int H, int D, int max_seq_len_hint, float scale,
+                          void *out, void *out_cross, dr_dtype out_dtype, int32_t *err_flag, void *stream) {
+    dr_status st = check_dims(B, H, D);
+    if (st != DR_OK) return st;
+    if (B > 32767) return DR_ERR_INVALID_ARG;   // self and cross rows share the grid's z dimension
+    int cap = 0;
+    st = check_cache(cache, &cap);
+    if (st != DR_OK) return st;
+    st = check_attn_args(q, seq_len, out, out_dtype, scale);
+    if (st != DR_OK) return st;
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return DR_ERR_INVALID_ARG;
+    if (!q_cross || !k_enc || !v_enc || !enc_len || !out_cross || Lc_max < 1) return DR_ERR_INVALID_ARG;
+    if (!aligned16(q_cross) || !aligned16(k_enc) || !aligned16(v_enc)) return DR_ERR_INVALID_ARG;
+    const bool paged = cache->layout == DR_KV_PAGED;
+    dr::AttnParams p;
+    fill_self(p, q, cache->k, cache->v, seq_len, paged ? cache->block_table : nullptr, B, H, cap,
+              paged ? cache->max_blocks_per_seq : 0, paged ? cache->num_blocks : 0, scale, out, out_dtype, err_flag);
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    p.xq = static_cast<const uint16_t *>(q_cross);
+    p.xk = static_cast<const uint16_t *>(k_enc);
+    p.xv = static_cast<const uint16_t *>(v_enc);
+    p.xlens = enc_len;
+    p.xcap = Lc_max;
+    p.xout = out_cross;
+    return launch(p, paged, max_seq_len_hint, stream);
 }
 
 dr_status dr_sample_topk_delayed(const float *logits, int B, int C, int V, int ldv, float temperature, int top_k,

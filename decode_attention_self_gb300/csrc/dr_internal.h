@@ -35,6 +35,17 @@ struct AttnParams {
     void *out;               // [B][H][64]
     int32_t out_f32;
     int32_t *err;
+    // Fused decode-layer launch only (see dr_decode_layer): this step's key and
+    // value, stored at position lens[b]-1 of the cache and used from registers,
+    // and a second set of B rows attending the description encoder's keys.
+    const uint16_t *k_new;   // [B][H][64] or null
+    const uint16_t *v_new;
+    const uint16_t *xq;      // cross rows: [B][H][64] or null (no cross rows)
+    const uint16_t *xk;      // [B][H][xcap][64]
+    const uint16_t *xv;
+    const int32_t *xlens;    // [B]
+    int32_t xcap;
+    void *xout;              // [B][H][64]
 };
 
 cudaError_t launch_decode_attn(const AttnParams &p, bool paged, int splits, cudaStream_t stream);

@@ -165,6 +165,29 @@ dr_status dr_decode_cross_attn(const void *q, const void *k_enc, const void *v_e
                                int32_t *err_flag, void *stream);
 
 /*
+ * dr_decode_layer -- one decoder layer's attention work of a decode step in
+ * one launch: the KV append, the self-attention and the cross-attention.
+ * Source: the same passages as the three calls above; fusing them is the
+ * launch-count reduction the page's profile motivates (Optimized Parler TTS,
+ * "Analysis and improvements": the decoder is overhead-bound, the GPU waits
+ * between small kernels).
+ *
+ * Equivalent to, in this order,
+ *   dr_kv_append(cache, k_new, v_new, pos = seq_len - 1, ...)
+ *   dr_decode_self_attn(q, cache, seq_len, ..., out, ...)
+ *   dr_decode_cross_attn(q_cross, k_enc, v_enc, enc_len, ..., Lc_max, ..., out_cross, ...)
+ * with results within the same tolerances (the key at seq_len[b]-1 is taken
+ * from k_new/v_new directly and also stored into the cache; rows whose
+ * seq_len is outside [1, capacity] are not appended and flag DR_ERRF_POS and
+ * DR_ERRF_SEQ_LEN).  Arguments are as for those calls; out and out_cross are
+ * both [B][H][D] in out_dtype.  B <= 32767.
+ */
+dr_status dr_decode_layer(const void *q, const dr_kv_cache *cache, const void *k_new, const void *v_new,
+                          const int32_t *seq_len, const void *q_cross, const void *k_enc, const void *v_enc,
+                          const int32_t *enc_len, int Lc_max, int B, int H, int D, int max_seq_len_hint, float scale,
+                          void *out, void *out_cross, dr_dtype out_dtype, int32_t *err_flag, void *stream);
+
+/*
  * dr_sample_topk_delayed -- one kernel that turns the logits of every
  * codebook of every row into this step's tokens.
  * Source: Optimized Parler TTS, "Future work" item 2 (temperature scaling,
