@@ -101,17 +101,22 @@ __device__ __forceinline__ void consume_tile(const uint4 (&kw)[4], const uint4 (
 // i.e. when occupancy is not what limits the bytes in flight.  Both variants
 // perform the same arithmetic in the same order.
 template <bool kPaged, bool kPipelined, bool kFused>
-__global__ void __launch_bounds__(kThreads, kPipelined ? 4 : (kFused ? 6 : 8)) decode_attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kernel(const AttnParams p) {
     __shared__ float s_wm[kWarps], s_wl[kWarps];
     __shared__ float s_wacc[kWarps][kD];
     __shared__ SoftmaxPartial s_part;
 
-    const int split = blockIdx.x;
-    const int nsplit = gridDim.x;
     const int h = blockIdx.y;
-    // Fused launches carry B self rows then B cross rows along z.
+    // Fused launches carry the B self rows along z, then the cross rows: split
+    // like the self rows (z = B + b), or packed one row per CTA (row b =
+    // (z - B) * gridDim.x + x) when a cross row is short enough for one CTA.
     const bool cross = kFused && p.xq != nullptr && (int)blockIdx.z >= p.B;
-    const int b = cross ? (int)blockIdx.z - p.B : (int)blockIdx.z;
+    const bool packed = cross && p.xpacked;
+    const int split = packed ? 0 : (int)blockIdx.x;
+    const int nsplit = packed ? 1 : (int)gridDim.x;
+    const int b = !cross ? (int)blockIdx.z
+                         : packed ? ((int)blockIdx.z - p.B) * (int)gridDim.x + (int)blockIdx.x : (int)blockIdx.z - p.B;
+    if (b >= p.B) return;   // tail of the packed region (no cluster barrier is reached there)
     const bool paged = kPaged && !cross;
     const uint16_t *qsrc = cross ? p.xq : p.q;
     const uint16_t *kcache = cross ? p.xk : p.k;
@@ -298,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : (kFused ? 6 : 8)) d
 template <bool kPaged, bool kPipelined, bool kFused>
 cudaError_t launch_variant(const AttnParams &p, int splits, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    const unsigned zrows = (unsigned)p.B * ((kFused && p.xq) ? 2u : 1u);
+    unsigned zrows = (unsigned)p.B;
+    if (kFused && p.xq) zrows += p.xpacked ? (unsigned)((p.B + splits - 1) / splits) : (unsigned)p.B;
     cfg.gridDim = dim3((unsigned)splits, (unsigned)p.H, zrows);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
@@ -323,7 +329,8 @@ constexpr int kPipelinedCtasPerSm = 4;
 
 template <bool kFused>
 cudaError_t launch_layout(const AttnParams &p, bool paged, int splits, cudaStream_t stream) {
-    const long long ctas = (long long)splits * p.H * p.B * ((kFused && p.xq) ? 2 : 1);
+    long long ctas = (long long)splits * p.H * p.B;
+    if (kFused && p.xq) ctas += (long long)p.H * (p.xpacked ? p.B : (long long)splits * p.B);
     const bool pipelined = ctas <= (long long)kPipelinedCtasPerSm * current_device_sms();
     if (paged)
         return pipelined ? launch_variant<true, true, kFused>(p, splits, stream)

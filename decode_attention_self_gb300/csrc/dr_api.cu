@@ -203,6 +203,11 @@ dr_status dr_decode_layer(const void *q, const dr_kv_cache *cache, const void *k
     p.xlens = enc_len;
     p.xcap = Lc_max;
     p.xout = out_cross;
+    // Cross rows that the standalone plan gives one CTA each are packed one per CTA;
+    // longer ones are split like the self rows.
+    const int sms = dr::current_device_sms();
+    if (sms <= 0) return DR_ERR_CUDA;
+    p.xpacked = dr_plan_splits(B, H, Lc_max, sms) == 1;
     return launch(p, paged, max_seq_len_hint, stream);
 }
 

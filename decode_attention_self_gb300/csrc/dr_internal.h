@@ -46,6 +46,7 @@ struct AttnParams {
     const int32_t *xlens;    // [B]
     int32_t xcap;
     void *xout;              // [B][H][64]
+    int32_t xpacked;         // 1: one CTA per cross row, gridDim.x rows per cluster; 0: rows split like self rows
 };
 
 cudaError_t launch_decode_attn(const AttnParams &p, bool paged, int splits, cudaStream_t stream);
