@@ -62,6 +62,10 @@ def lib():
         L.oracle_sample.argtypes = [_f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                     ctypes.c_int, _u64p, _i32p, ctypes.c_int32, _i32p, _f64p, _f64p, _i32p]
         L.oracle_sample.restype = ctypes.c_int
+        L.oracle_embed_tokens.argtypes = [_i32p, _u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64p]
+        L.oracle_embed_tokens.restype = ctypes.c_int
+        L.oracle_lm_head.argtypes = [_u16p, _u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64p]
+        L.oracle_lm_head.restype = None
         _lib = L
     return _lib
 
@@ -212,3 +216,25 @@ def sample(logits, temperature, top_k, seeds, steps, pad_id, V=None, want_probs=
     if rc:
         raise ValueError("invalid sampler input")
     return dict(tokens=tokens, margins=margins, probs=probs, topk=topk)
+
+
+def embed_tokens(tokens, table, V):
+    """tokens [B,C] int; table [C*V, Dm] bf16 bits. Returns [B, Dm] float64 (sum of the C embeddings)."""
+    tk = _i32(tokens)
+    tb = _u16(table)
+    B, C = tk.shape
+    Dm = tb.shape[1]
+    out = np.zeros((B, Dm), np.float64)
+    if lib().oracle_embed_tokens(_p(tk, _i32p), _p(tb, _u16p), B, C, V, Dm, _p(out, _f64p)):
+        raise ValueError("token outside the vocabulary")
+    return out
+
+
+def lm_head(hidden, W):
+    """hidden [B,K], W [N,K] (bf16 bits). Returns [B,N] float64 logits."""
+    h, w = _u16(hidden), _u16(W)
+    B, K = h.shape
+    N = w.shape[0]
+    out = np.zeros((B, N), np.float64)
+    lib().oracle_lm_head(_p(h, _u16p), _p(w, _u16p), B, K, N, _p(out, _f64p))
+    return out

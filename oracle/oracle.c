@@ -353,3 +353,42 @@ int oracle_sample(const float *logits, int B, int C, int V, int ldv, float tempe
         }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Merged codebook embedding lookup (Optimized Parler TTS, "Analysis    */
+/* and improvements", other optimizations item 3: the nine embedding    */
+/* lookups merged into one).  The decoder input of the next step is the */
+/* sum over codebooks of each codebook's embedding of its token:        */
+/*   x[b][d] = sum_c table[c*V + tokens[b][c]][d]                        */
+/* table: [C*V][Dm] bf16 (codebook c's rows at c*V); tokens: [B][C].     */
+/* Returns 0, or -1 when a token is outside [0, V).                     */
+/* ------------------------------------------------------------------ */
+int oracle_embed_tokens(const int32_t *tokens, const uint16_t *table, int B, int C, int V, int Dm, double *out) {
+    for (int b = 0; b < B; ++b) {
+        for (int d = 0; d < Dm; ++d) out[(size_t)b * Dm + d] = 0.0;
+        for (int c = 0; c < C; ++c) {
+            int32_t t = tokens[(size_t)b * C + c];
+            if (t < 0 || t >= V) return -1;
+            const uint16_t *row = table + ((size_t)c * V + (size_t)t) * Dm;
+            for (int d = 0; d < Dm; ++d) out[(size_t)b * Dm + d] += oracle_bf16_to_double(row[d]);
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Merged LM head on the last position (same page, other optimizations  */
+/* items 1-2: the head evaluated only for the newest position, and the  */
+/* nine codebook heads merged into one weight matrix):                  */
+/*   logits[b][n] = sum_k hidden[b][k] * W[n][k],  n = c*V + v           */
+/* hidden: [B][K] bf16; W: [N][K] bf16; out: [B][N] doubles.            */
+/* ------------------------------------------------------------------ */
+void oracle_lm_head(const uint16_t *hidden, const uint16_t *W, int B, int K, int N, double *out) {
+    for (int b = 0; b < B; ++b)
+        for (int n = 0; n < N; ++n) {
+            double s = 0.0;
+            for (int k = 0; k < K; ++k)
+                s += oracle_bf16_to_double(hidden[(size_t)b * K + k]) * oracle_bf16_to_double(W[(size_t)n * K + k]);
+            out[(size_t)b * N + n] = s;
+        }
+}
