@@ -199,6 +199,19 @@ class DeviceStep:
         self.out_x = torch.empty_like(self.out_s)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.hint = int(w.seq_len.max())
+        # the decoder's output and input ends (not part of the timed step): merged LM head and
+        # merged embedding lookup, synthetic weights [C*V, 1024] bf16
+        self.hidden = W.randn_bf16((w.B, 1024), dev, w.index, 500 + rank)
+        self.w_head = (W.randn_bf16((w.C * w.V, 1024), dev, w.index, 501) * 0.1).contiguous()
+        self.w_emb = W.randn_bf16((w.C * w.V, 1024), dev, w.index, 502)
+        self.head_logits = torch.empty((w.B, w.C, w.ldv), dtype=torch.float32, device=dev)
+        self.emb_out = torch.empty((w.B, 1024), dtype=torch.bfloat16, device=dev)
+
+    def run_lm_head(self):
+        self.api.dr_lm_head(self.hidden, self.w_head, self.w.C, self.head_logits)
+
+    def run_embed(self):
+        self.api.dr_embed_tokens(self.tokens, self.w_emb, self.w.V, self.emb_out, err_flag=self.err)
 
     def launches_per_step(self) -> int:
         return (1 if self.fused else 3) * self.w.layers + 1
@@ -423,7 +436,15 @@ def main():
         for _ in range(K):
             ds.run_sampler_only()
 
-    regions = {"step": steps, "self": self_only, "sampler": sampler_only}
+    def head_only():
+        for _ in range(K):
+            ds.run_lm_head()
+
+    def embed_only():
+        for _ in range(K):
+            ds.run_embed()
+
+    regions = {"step": steps, "self": self_only, "sampler": sampler_only, "lm_head": head_only, "embed": embed_only}
     graphs = {k: capture(f) for k, f in regions.items()} if not args.eager else None
 
     def timed(name):
@@ -443,6 +464,8 @@ def main():
         step_total_ms = timed("step")
         self_total_ms = timed("self")
         samp_total_ms = timed("sampler")
+        head_total_ms = timed("lm_head")
+        emb_total_ms = timed("embed")
     barrier(dist)
     ms = max_over_ranks(dist, step_total_ms / K, dev)
     self_avg_ms = self_total_ms / (K * w.layers)
@@ -499,6 +522,10 @@ def main():
                 "us_per_step": ms * 1e3, "layer_us" if ds.fused else "self_attn_us": self_avg_ms * 1e3,
                 "sampler_us": samp_avg_ms * 1e3,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "decoder_ends": {
+                    "lm_head": {"us": head_total_ms / K * 1e3, "batch": w.B, "K": 1024, "N": w.C * w.V,
+                                "weight_GBps": w.C * w.V * 1024 * 2 / (head_total_ms / K * 1e-3) / 1e9},
+                    "embed": {"us": emb_total_ms / K * 1e3, "rows_gathered": w.B * w.C, "Dm": 1024}},
                 "gpu_launches": ds.launches_per_step() * K, "launch_mode": mode,
                 "kernel_timing": "dominant kernel and sampler: K x layers (K) launches of the timed steps, "
                                  "back to back in their own graph, events around it",

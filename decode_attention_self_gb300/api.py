@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_PKG, "libdecoderattn.so")
 DR_OK, DR_ERR_INVALID_ARG, DR_ERR_UNSUPPORTED, DR_ERR_CUDA = 0, 1, 2, 3
 DR_KV_CONTIGUOUS, DR_KV_PAGED = 0, 1
 DR_BF16, DR_F32 = 0, 1
-DR_ERRF_SEQ_LEN, DR_ERRF_BLOCK_ID, DR_ERRF_POS = 1, 2, 4
+DR_ERRF_SEQ_LEN, DR_ERRF_BLOCK_ID, DR_ERRF_POS, DR_ERRF_TOKEN = 1, 2, 4, 8
 DR_SAMPLE_ADVANCE = 1
 
 if not os.path.exists(LIB_PATH):
@@ -44,12 +44,14 @@ _lib.dr_decode_cross_attn.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _v
 _lib.dr_decode_layer.argtypes = [_vp, ctypes.POINTER(dr_kv_cache), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
                                  _i, _f, _vp, _vp, _i, _vp, _vp]
 _lib.dr_sample_topk_delayed.argtypes = [_vp, _i, _i, _i, _i, _f, _i, _vp, _vp, ctypes.c_int32, _vp, _vp, _i, _vp]
+_lib.dr_embed_tokens.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _i, _vp, _vp]
+_lib.dr_lm_head.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]
 _lib.dr_plan_splits.argtypes = [_i, _i, _i, _i]
 _lib.dr_plan_splits.restype = _i
 _lib.dr_status_string.argtypes = [_i]
 _lib.dr_status_string.restype = ctypes.c_char_p
 for _fn in ("dr_kv_append", "dr_decode_self_attn", "dr_decode_cross_attn", "dr_decode_layer",
-            "dr_sample_topk_delayed"):
+            "dr_sample_topk_delayed", "dr_embed_tokens", "dr_lm_head"):
     getattr(_lib, _fn).restype = _i
 
 
@@ -199,6 +201,29 @@ def dr_sample_topk_delayed(logits: torch.Tensor, temperature: float, top_k: int,
                                        _ptr(probs, torch.float32, "probs"), DR_SAMPLE_ADVANCE if advance else 0,
                                        _stream(stream)))
     return tokens
+
+
+def dr_embed_tokens(tokens: torch.Tensor, table: torch.Tensor, V: int, out: torch.Tensor,
+                    err_flag: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[b] = sum_c table[c*V + tokens[b,c]]; tokens [B,C] int32, table [C*V, Dm] bf16, out [B,Dm]."""
+    B, C = tokens.shape
+    Dm = table.shape[1]
+    od = DR_F32 if out.dtype == torch.float32 else DR_BF16
+    _check("dr_embed_tokens",
+           _lib.dr_embed_tokens(_ptr(tokens, torch.int32, "tokens"), _ptr(table, torch.bfloat16, "table"), B, C, V, Dm,
+                                _ptr(out, None, "out"), od, _ptr(err_flag, torch.int32, "err_flag"), _stream(stream)))
+    return out
+
+
+def dr_lm_head(hidden: torch.Tensor, W: torch.Tensor, C: int, logits: torch.Tensor, stream=None) -> torch.Tensor:
+    """logits [B,C,ldv] float32 from hidden [B,K] bf16 and merged heads W [C*V, K] bf16 (V = W rows / C)."""
+    B, K = hidden.shape
+    V = W.shape[0] // C
+    ldv = logits.shape[2]
+    _check("dr_lm_head",
+           _lib.dr_lm_head(_ptr(hidden, torch.bfloat16, "hidden"), _ptr(W, torch.bfloat16, "W"), B, K, C, V, ldv,
+                           _ptr(logits, torch.float32, "logits"), _stream(stream)))
+    return logits
 
 
 def loaded_library_path() -> str:

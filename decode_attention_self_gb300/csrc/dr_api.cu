@@ -237,6 +237,43 @@ dr_status dr_sample_topk_delayed(const float *logits, int B, int C, int V, int l
     return from_cuda(dr::launch_sample(p, static_cast<cudaStream_t>(stream)));
 }
 
+dr_status dr_embed_tokens(const int32_t *tokens, const void *table, int B, int C, int V, int Dm, void *out,
+                          dr_dtype out_dtype, int32_t *err_flag, void *stream) {
+    if (!tokens || !table || !out || !aligned16(table) || !aligned16(out)) return DR_ERR_INVALID_ARG;
+    if (B < 1 || B > 0x7FFFFFFF || C < 1 || V < 1 || Dm < 8 || Dm % 8 != 0) return DR_ERR_INVALID_ARG;
+    if (out_dtype != DR_BF16 && out_dtype != DR_F32) return DR_ERR_INVALID_ARG;
+    dr::EmbedParams p;
+    p.tokens = tokens;
+    p.table = static_cast<const uint16_t *>(table);
+    p.out = out;
+    p.B = B;
+    p.C = C;
+    p.V = V;
+    p.Dm = Dm;
+    p.out_f32 = out_dtype == DR_F32;
+    p.err = err_flag;
+    return from_cuda(dr::launch_embed_tokens(p, static_cast<cudaStream_t>(stream)));
+}
+
+dr_status dr_lm_head(const void *hidden, const void *W, int B, int K, int C, int V, int ldv, float *logits,
+                     void *stream) {
+    if (!hidden || !W || !logits || !aligned16(hidden) || !aligned16(W)) return DR_ERR_INVALID_ARG;
+    if (B < 1 || C < 1 || V < 1 || ldv < V || K < 1) return DR_ERR_INVALID_ARG;
+    if ((long long)C * V > 0x7FFFFFFFLL) return DR_ERR_INVALID_ARG;
+    const int kc = K / 256;
+    if (K % 256 != 0 || !(kc == 1 || kc == 2 || kc == 3 || kc == 4 || kc == 6 || kc == 8)) return DR_ERR_UNSUPPORTED;
+    dr::LmHeadParams p;
+    p.hidden = static_cast<const uint16_t *>(hidden);
+    p.W = static_cast<const uint16_t *>(W);
+    p.logits = logits;
+    p.B = B;
+    p.K = K;
+    p.C = C;
+    p.V = V;
+    p.ldv = ldv;
+    return from_cuda(dr::launch_lm_head(p, static_cast<cudaStream_t>(stream)));
+}
+
 const char *dr_status_string(dr_status s) {
     switch (s) {
         case DR_OK: return "ok";

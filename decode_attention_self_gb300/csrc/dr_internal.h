@@ -74,4 +74,23 @@ struct SampleParams {
 
 cudaError_t launch_sample(const SampleParams &p, cudaStream_t stream);
 
+struct EmbedParams {
+    const int32_t *tokens;   // [B][C]
+    const uint16_t *table;   // [C*V][Dm] bf16
+    void *out;               // [B][Dm] bf16 or f32
+    int32_t B, C, V, Dm, out_f32;
+    int32_t *err;
+};
+
+cudaError_t launch_embed_tokens(const EmbedParams &p, cudaStream_t stream);
+
+struct LmHeadParams {
+    const uint16_t *hidden;  // [B][K] bf16
+    const uint16_t *W;       // [C*V][K] bf16
+    float *logits;           // [B][C][ldv]
+    int32_t B, K, C, V, ldv;
+};
+
+cudaError_t launch_lm_head(const LmHeadParams &p, cudaStream_t stream);
+
 }  // namespace dr

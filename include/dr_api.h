@@ -64,6 +64,7 @@ typedef enum dr_dtype { DR_BF16 = 0, DR_F32 = 1 } dr_dtype;
 #define DR_ERRF_SEQ_LEN 1  /* a seq_len / enc_len entry outside [1, capacity]; it was clamped */
 #define DR_ERRF_BLOCK_ID 2 /* a needed block-table entry outside [0, num_blocks); its keys were skipped */
 #define DR_ERRF_POS 4      /* an append position outside [0, capacity) or on an unmapped block; row skipped */
+#define DR_ERRF_TOKEN 8    /* a token outside [0, V) in dr_embed_tokens; that codebook's row was skipped */
 
 /* Sampler flags. */
 #define DR_SAMPLE_ADVANCE 1 /* after drawing, step[b] += 1 for every row b */
@@ -226,6 +227,40 @@ dr_status dr_decode_layer(const void *q, const dr_kv_cache *cache, const void *k
 dr_status dr_sample_topk_delayed(const float *logits, int B, int C, int V, int ldv, float temperature, int top_k,
                                  const uint64_t *seeds, int32_t *step, int32_t pad_id, int32_t *tokens, float *probs,
                                  int flags, void *stream);
+
+/*
+ * dr_embed_tokens -- the next step's decoder input from this step's tokens:
+ *   out[b][d] = sum_{c=0..C-1} table[c*V + tokens[b][c]][d]
+ * Source: Optimized Parler TTS, "Analysis and improvements", other
+ * optimizations item 3: the nine codebook embedding lookups merged into one
+ * (one merged table, one gather of C rows per batch row).
+ *
+ *   tokens : [B][C] int32 (device), e.g. the tokens dr_sample_topk_delayed wrote
+ *   table  : [C*V][Dm] bf16 (device, 16-byte aligned); codebook c's rows start at c*V
+ *   out    : [B][Dm] in out_dtype (device, 16-byte aligned); fp32 sum in c order
+ *   Dm     : a multiple of 8
+ *   err_flag : nullable; DR_ERRF_TOKEN when a token is outside [0, V) (that
+ *            term is left out of the sum)
+ */
+dr_status dr_embed_tokens(const int32_t *tokens, const void *table, int B, int C, int V, int Dm, void *out,
+                          dr_dtype out_dtype, int32_t *err_flag, void *stream);
+
+/*
+ * dr_lm_head -- logits of the newest position from the merged codebook heads:
+ *   logits[b][c][v] = sum_k hidden[b][k] * W[c*V + v][k]
+ * Source: Optimized Parler TTS, "Analysis and improvements", other
+ * optimizations items 1-2: the LM head computed for the last position only,
+ * and the nine codebook heads merged into one weight matrix.
+ *
+ *   hidden : [B][K] bf16 (device, 16-byte aligned), the newest position's hidden state
+ *   W      : [C*V][K] bf16 (device, 16-byte aligned)
+ *   logits : [B][C][ldv] float32 (device), ldv >= V; columns [V, ldv) untouched.
+ *            The layout dr_sample_topk_delayed reads.
+ *   K      : 256, 512, 768, 1024, 1536 or 2048 (DR_ERR_UNSUPPORTED otherwise)
+ * fp32 accumulation; each logit is one dot product in a fixed order.
+ */
+dr_status dr_lm_head(const void *hidden, const void *W, int B, int K, int C, int V, int ldv, float *logits,
+                     void *stream);
 
 /*
  * dr_plan_splits -- host-only query: how many CTAs (one thread-block
