@@ -66,6 +66,26 @@ def lib():
         L.oracle_embed_tokens.restype = ctypes.c_int
         L.oracle_lm_head.argtypes = [_u16p, _u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64p]
         L.oracle_lm_head.restype = None
+        _u8p = ctypes.POINTER(ctypes.c_uint8)
+        L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_to_double.restype = ctypes.c_double
+        L.oracle_double_to_e4m3.argtypes = [ctypes.c_double]
+        L.oracle_double_to_e4m3.restype = ctypes.c_uint8
+        L.oracle_kv_append_fp8_contiguous.argtypes = [_u8p, _u8p, _u16p, _u16p, _i32p, ctypes.c_int, ctypes.c_int,
+                                                      ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float]
+        L.oracle_kv_append_fp8_contiguous.restype = None
+        L.oracle_kv_append_fp8_paged.argtypes = [_u8p, _u8p, _i32p, ctypes.c_int, ctypes.c_int, _u16p, _u16p, _i32p,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                                 ctypes.c_float]
+        L.oracle_kv_append_fp8_paged.restype = None
+        L.oracle_attn_fp8_contiguous.argtypes = [_u16p, _u8p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, _i32p, ctypes.c_double, ctypes.c_double,
+                                                 ctypes.c_double, _f64p]
+        L.oracle_attn_fp8_contiguous.restype = None
+        L.oracle_attn_fp8_paged.argtypes = [_u16p, _u8p, _u8p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_double,
+                                            ctypes.c_double, ctypes.c_double, _f64p]
+        L.oracle_attn_fp8_paged.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -237,4 +257,63 @@ def lm_head(hidden, W):
     N = w.shape[0]
     out = np.zeros((B, N), np.float64)
     lib().oracle_lm_head(_p(h, _u16p), _p(w, _u16p), B, K, N, _p(out, _f64p))
+    return out
+
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+
+
+def _u8(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint8, a.dtype
+    return a
+
+
+def e4m3_to_double(code: int) -> float:
+    return lib().oracle_e4m3_to_double(int(code))
+
+
+def double_to_e4m3(x: float) -> int:
+    return int(lib().oracle_double_to_e4m3(float(x)))
+
+
+def kv_append_fp8_contiguous(k, v, k_new, v_new, pos, k_scale, v_scale):
+    """In-place quantising append into host fp8 caches k, v [B,H,max_len,D] (uint8 codes)."""
+    k_new, v_new = _u16(k_new), _u16(v_new)
+    B, H, max_len, D = k.shape
+    ps = _i32(pos)
+    lib().oracle_kv_append_fp8_contiguous(_p(k, _u8p), _p(v, _u8p), _p(k_new, _u16p), _p(v_new, _u16p),
+                                          _p(ps, _i32p), B, H, D, max_len, k_scale, v_scale)
+
+
+def kv_append_fp8_paged(k_pool, v_pool, block_table, k_new, v_new, pos, k_scale, v_scale, block_size=16):
+    k_new, v_new = _u16(k_new), _u16(v_new)
+    bt = _i32(block_table)
+    ps = _i32(pos)
+    B, H, D = k_new.shape
+    lib().oracle_kv_append_fp8_paged(_p(k_pool, _u8p), _p(v_pool, _u8p), _p(bt, _i32p), bt.shape[1], block_size,
+                                     _p(k_new, _u16p), _p(v_new, _u16p), _p(ps, _i32p), B, H, D, k_scale, v_scale)
+
+
+def attn_fp8_contiguous(q, k, v, seq_len, scale, k_scale, v_scale):
+    q, k, v = _u16(q), _u8(k), _u8(v)
+    B, H, max_len, D = k.shape
+    sl = _i32(seq_len)
+    out = np.zeros((B, H, D), np.float64)
+    lib().oracle_attn_fp8_contiguous(_p(q, _u16p), _p(k, _u8p), _p(v, _u8p), B, H, D, max_len, _p(sl, _i32p), scale,
+                                     k_scale, v_scale, _p(out, _f64p))
+    return out
+
+
+def attn_fp8_paged(q, k_pool, v_pool, block_table, seq_len, scale, k_scale, v_scale, block_size=16):
+    q, k_pool, v_pool = _u16(q), _u8(k_pool), _u8(v_pool)
+    bt = _i32(block_table)
+    sl = _i32(seq_len)
+    B, H, D = q.shape
+    out = np.zeros((B, H, D), np.float64)
+    rc = lib().oracle_attn_fp8_paged(_p(q, _u16p), _p(k_pool, _u8p), _p(v_pool, _u8p), _p(bt, _i32p), bt.shape[1],
+                                     k_pool.shape[0], block_size, B, H, D, _p(sl, _i32p), scale, k_scale, v_scale,
+                                     _p(out, _f64p))
+    if rc:
+        raise ValueError("block table entry outside the pool")
     return out

@@ -392,3 +392,145 @@ void oracle_lm_head(const uint16_t *hidden, const uint16_t *W, int B, int K, int
             out[(size_t)b * N + n] = s;
         }
 }
+
+/* ------------------------------------------------------------------ */
+/* FP8 E4M3 KV cache (the page's "Future work" item 1 asks for a cache  */
+/* that loads memory bandwidth less; an 8-bit KV format halves the      */
+/* bytes).  E4M3 follows the OCP 8-bit floating point specification:    */
+/* 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0    */
+/* holds subnormals m/8 * 2^-6; S.1111.111 is NaN; no infinities; the   */
+/* largest finite magnitude is 1.75 * 2^8 = 448.                        */
+/* ------------------------------------------------------------------ */
+double oracle_e4m3_to_double(uint8_t c) {
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = (m / 8.0) * ldexp(1.0, -6);
+    else v = (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Round to the nearest E4M3 value, ties to the even code (mantissa LSB 0), */
+/* magnitudes at or above 448 saturating to 448 (the "satfinite" rule),     */
+/* NaN to 0x7F.  Brute force over the 127 non-negative finite codes.        */
+uint8_t oracle_double_to_e4m3(double x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    uint8_t best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double d = fabs(oracle_e4m3_to_double((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+            best = (uint8_t)c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* Quantising append: code = E4M3(fl32(x / scale)) with x the bf16 value   */
+/* (binary32 division, round to nearest).  k_new/v_new [B][H][D] bf16;    */
+/* contiguous fp8 cache [B][H][max_len][D].                                */
+static uint8_t quantize(uint16_t bf16, float scale) {
+    volatile float q = (float)oracle_bf16_to_double(bf16) / scale;
+    return oracle_double_to_e4m3((double)q);
+}
+
+void oracle_kv_append_fp8_contiguous(uint8_t *k, uint8_t *v, const uint16_t *k_new, const uint16_t *v_new,
+                                     const int32_t *pos, int B, int H, int D, int max_len, float k_scale,
+                                     float v_scale) {
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            size_t row = (size_t)b * H + h;
+            size_t dst = (row * (size_t)max_len + (size_t)pos[b]) * D;
+            for (int e = 0; e < D; ++e) {
+                k[dst + e] = quantize(k_new[row * D + e], k_scale);
+                v[dst + e] = quantize(v_new[row * D + e], v_scale);
+            }
+        }
+}
+
+void oracle_kv_append_fp8_paged(uint8_t *k_pool, uint8_t *v_pool, const int32_t *block_table,
+                                int max_blocks_per_seq, int block_size, const uint16_t *k_new,
+                                const uint16_t *v_new, const int32_t *pos, int B, int H, int D, float k_scale,
+                                float v_scale) {
+    for (int b = 0; b < B; ++b) {
+        int32_t blk = block_table[(size_t)b * max_blocks_per_seq + pos[b] / block_size];
+        int slot = pos[b] % block_size;
+        for (int h = 0; h < H; ++h) {
+            size_t row = (size_t)b * H + h;
+            size_t dst = (((size_t)blk * H + h) * block_size + (size_t)slot) * D;
+            for (int e = 0; e < D; ++e) {
+                k_pool[dst + e] = quantize(k_new[row * D + e], k_scale);
+                v_pool[dst + e] = quantize(v_new[row * D + e], v_scale);
+            }
+        }
+    }
+}
+
+/* Attention over n fp8 keys/values: k_j = decode(code) * k_scale,       */
+/* v_j = decode(code) * v_scale; then the plain definition as above.     */
+void oracle_attend_fp8(const uint16_t *q, const uint8_t *keys, const uint8_t *values, int64_t n, int d,
+                       double scale, double k_scale, double v_scale, double *out) {
+    for (int e = 0; e < d; ++e) out[e] = 0.0;
+    if (n <= 0) return;
+    double *s = (double *)malloc((size_t)n * sizeof(double));
+    double smax = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+        double dot = 0.0;
+        for (int e = 0; e < d; ++e)
+            dot += oracle_bf16_to_double(q[e]) * (oracle_e4m3_to_double(keys[j * d + e]) * k_scale);
+        s[j] = scale * dot;
+        if (s[j] > smax) smax = s[j];
+    }
+    double denom = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        s[j] = exp(s[j] - smax);
+        denom += s[j];
+    }
+    for (int64_t j = 0; j < n; ++j) {
+        double p = s[j] / denom;
+        for (int e = 0; e < d; ++e) out[e] += p * (oracle_e4m3_to_double(values[j * d + e]) * v_scale);
+    }
+    free(s);
+}
+
+void oracle_attn_fp8_contiguous(const uint16_t *q, const uint8_t *k, const uint8_t *v, int B, int H, int D,
+                                int max_len, const int32_t *seq_len, double scale, double k_scale, double v_scale,
+                                double *out) {
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            size_t row = (size_t)b * H + h;
+            oracle_attend_fp8(q + row * D, k + row * (size_t)max_len * D, v + row * (size_t)max_len * D, seq_len[b],
+                              D, scale, k_scale, v_scale, out + row * D);
+        }
+}
+
+int oracle_attn_fp8_paged(const uint16_t *q, const uint8_t *k_pool, const uint8_t *v_pool, const int32_t *block_table,
+                          int max_blocks_per_seq, int num_blocks, int block_size, int B, int H, int D,
+                          const int32_t *seq_len, double scale, double k_scale, double v_scale, double *out) {
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            size_t row = (size_t)b * H + h;
+            int n = seq_len[b];
+            uint8_t *kg = (uint8_t *)malloc((size_t)(n > 0 ? n : 1) * D);
+            uint8_t *vg = (uint8_t *)malloc((size_t)(n > 0 ? n : 1) * D);
+            for (int j = 0; j < n; ++j) {
+                int32_t blk = block_table[(size_t)b * max_blocks_per_seq + j / block_size];
+                if (blk < 0 || blk >= num_blocks) {
+                    free(kg);
+                    free(vg);
+                    return -1;
+                }
+                size_t src = (((size_t)blk * H + h) * block_size + (size_t)(j % block_size)) * D;
+                memcpy(kg + (size_t)j * D, k_pool + src, (size_t)D);
+                memcpy(vg + (size_t)j * D, v_pool + src, (size_t)D);
+            }
+            oracle_attend_fp8(q + row * D, kg, vg, n, D, scale, k_scale, v_scale, out + row * D);
+            free(kg);
+            free(vg);
+        }
+    return 0;
+}
