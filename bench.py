@@ -47,14 +47,15 @@ NOMINAL_HBM_GBS = 8000.0
 # ---------------------------------------------------------------------------
 # bytes the step must move (algorithmic, not measured)
 # ---------------------------------------------------------------------------
-def step_bytes(w: W.Workload, out_bytes: int = 2):
+def step_bytes(w: W.Workload, out_bytes: int = 2, kv_bytes: int = 2):
+    """Bytes one decode step must move; kv_bytes is the self cache's element size (2 bf16, 1 e4m3)."""
     BHD = w.B * w.H * w.D
     L = w.seq_len.astype(np.int64)
-    self_b = int(4 * w.H * w.D * L.sum()) + BHD * 2 + BHD * out_bytes
+    self_b = int(2 * kv_bytes * w.H * w.D * L.sum()) + BHD * 2 + BHD * out_bytes
     if w.layout == "paged":
         self_b += int(4 * ((L + 15) // 16).sum())
     cross_b = int(4 * w.H * w.D * w.enc_len.astype(np.int64).sum()) + BHD * 2 + BHD * out_bytes
-    append_b = 4 * BHD * 2                                # k_new, v_new read; two rows written
+    append_b = 2 * BHD * 2 + 2 * BHD * kv_bytes          # k_new, v_new read; two rows written
     sampler_b = w.B * w.C * w.V * 4 + w.B * w.C * 4
     per_layer = self_b + cross_b + append_b
     return dict(self=self_b, cross=cross_b, append=append_b, sampler=sampler_b,
@@ -177,14 +178,15 @@ class DeviceStep:
     """One decode step on the GPU: per layer one fused dr_decode_layer launch (append + self + cross), or with
     fused=False the three separate calls; then dr_sample_topk_delayed once."""
 
-    def __init__(self, w: W.Workload, dev, rank: int, fused: bool = True):
+    def __init__(self, w: W.Workload, dev, rank: int, fused: bool = True, fp8: bool = False):
         from decode_attention_self_gb300 import api
 
         self.api, self.w, self.dev, self.fused = api, w, dev, fused
         self.layers = []
         for l in range(w.layers):
-            c = W.make_self_cache(w, 1000 * rank + l, device=dev)
-            kv = api.KVCache(c.k, c.v, c.block_table.to(dev) if c.block_table is not None else None)
+            c = (W.make_self_cache_fp8 if fp8 else W.make_self_cache)(w, 1000 * rank + l, device=dev)
+            kv = api.KVCache(c.k, c.v, c.block_table.to(dev) if c.block_table is not None else None, c.k_scale,
+                             c.v_scale)
             kx, vx = W.make_cross_kv(w, 1000 * rank + l, device=dev)
             q, qx, kn, vn = W.make_step_inputs(w, 1000 * rank + l, device=dev)
             self.layers.append(dict(kv=kv, kx=kx, vx=vx, q=q, qx=qx, kn=kn, vn=vn))
@@ -363,6 +365,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps one by one instead of a CUDA graph")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="self-attention cache format (fp8 = OCP E4M3 codes with per-layer scales)")
     ap.add_argument("--unfused", action="store_true",
                     help="three launches per layer (append, self, cross) instead of one dr_decode_layer launch")
     args = ap.parse_args()
@@ -370,9 +374,9 @@ def main():
     w = W.make_workload(args.workload)
     if args.layers > 0:
         w = dataclasses.replace(w, layers=args.layers)
-    sb = step_bytes(w)
+    sb = step_bytes(w, kv_bytes=1 if args.kv == "fp8" else 2)
     config = {"workload": f"{w.index}: {w.name}", "batch": w.B, "layers": w.layers,
-              "heads": w.H, "head_dim": w.D, "kv_layout": w.layout, "kv_dtype": "bf16", "codebooks": w.C,
+              "heads": w.H, "head_dim": w.D, "kv_layout": w.layout, "kv_dtype": "e4m3" if args.kv == "fp8" else "bf16", "codebooks": w.C,
               "vocab": w.V, "top_k": w.top_k, "temperature": w.temperature,
               "self_len_mean": float(w.seq_len.mean()), "self_len_max": int(w.seq_len.max()),
               "cross_len_mean": float(w.enc_len.mean()), "parallelism": f"replicas x{ws}",
@@ -397,7 +401,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist = init_dist(ws, "nccl")
-    ds = DeviceStep(w, dev, rank, fused=not args.unfused)
+    ds = DeviceStep(w, dev, rank, fused=not args.unfused, fp8=args.kv == "fp8")
     torch.cuda.synchronize()
 
     for _ in range(max(3, args.warmup)):

@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(_PKG, "libdecoderattn.so")
 DR_OK, DR_ERR_INVALID_ARG, DR_ERR_UNSUPPORTED, DR_ERR_CUDA = 0, 1, 2, 3
 DR_KV_CONTIGUOUS, DR_KV_PAGED = 0, 1
 DR_BF16, DR_F32 = 0, 1
+DR_KV_BF16, DR_KV_FP8_E4M3 = 0, 1
 DR_ERRF_SEQ_LEN, DR_ERRF_BLOCK_ID, DR_ERRF_POS, DR_ERRF_TOKEN = 1, 2, 4, 8
 DR_SAMPLE_ADVANCE = 1
 
@@ -33,8 +34,9 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 class dr_kv_cache(ctypes.Structure):
     _fields_ = [("layout", ctypes.c_int32), ("max_len", ctypes.c_int32), ("block_size", ctypes.c_int32),
-                ("num_blocks", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("block_table", ctypes.c_void_p)]
+                ("num_blocks", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+                ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 _vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
@@ -95,13 +97,19 @@ def _stream(stream) -> int | None:
 class KVCache:
     """One layer's self-attention cache (device tensors owned by the caller).
 
-    contiguous: k, v [B, H, max_len, D] bf16.
-    paged:      k, v [num_blocks, H, 16, D] bf16 and block_table [B, max_blocks] int32.
+    contiguous: k, v [B, H, max_len, D] bf16, or uint8 e4m3 codes with k_scale/v_scale.
+    paged:      k, v [num_blocks, H, 16, D] (same element formats) and block_table [B, max_blocks] int32.
     """
 
     k: torch.Tensor
     v: torch.Tensor
     block_table: torch.Tensor | None = None
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    @property
+    def fp8(self) -> bool:
+        return self.k.dtype == torch.uint8
 
     @property
     def paged(self) -> bool:
@@ -113,8 +121,12 @@ class KVCache:
 
     def as_c(self) -> dr_kv_cache:
         c = dr_kv_cache()
-        c.k = _ptr(self.k, torch.bfloat16, "cache.k")
-        c.v = _ptr(self.v, torch.bfloat16, "cache.v")
+        dt = torch.uint8 if self.fp8 else torch.bfloat16
+        c.k = _ptr(self.k, dt, "cache.k")
+        c.v = _ptr(self.v, dt, "cache.v")
+        c.kv_dtype = DR_KV_FP8_E4M3 if self.fp8 else DR_KV_BF16
+        c.k_scale = float(self.k_scale)
+        c.v_scale = float(self.v_scale)
         if self.paged:
             c.layout = DR_KV_PAGED
             c.block_size = self.k.shape[2]

@@ -25,6 +25,9 @@
 // the kernel is bound by HBM bandwidth; there is no dense contraction for the
 // tensor cores (one query row).
 #include <cooperative_groups.h>
+#include <cuda_fp8.h>
+
+#include <type_traits>
 
 #include "dr_device.cuh"
 #include "dr_internal.h"
@@ -45,6 +48,30 @@ struct SoftmaxPartial {
     float acc[kD];   // sum of 2^(s - m) * v
 };
 
+// Storage formats of a KV cache.  One lane moves the 8 consecutive dims of one
+// key that it owns: 16 bytes of bf16 or 8 bytes of e4m3 codes.
+struct Bf16Kv {
+    using Chunk = uint4;
+    static constexpr int kElemBytes = 2;
+    __device__ static Chunk zero() { return make_uint4(0, 0, 0, 0); }
+    __device__ static Chunk load(const uint8_t *p) { return ld_stream16(p); }
+    __device__ static void store(uint8_t *p, const Chunk &c) { *reinterpret_cast<uint4 *>(p) = c; }
+    __device__ static void unpack(const Chunk &c, float (&f)[8]) { unpack8(c, f); }
+    // This step's key/value (bf16) in the cache's format.
+    __device__ static Chunk from_bf16(const uint4 &w, float) { return w; }
+};
+
+struct Fp8Kv {
+    using Chunk = uint2;
+    static constexpr int kElemBytes = 1;
+    __device__ static Chunk zero() { return make_uint2(0, 0); }
+    __device__ static Chunk load(const uint8_t *p) { return ld_stream8(p); }
+    __device__ static void store(uint8_t *p, const Chunk &c) { *reinterpret_cast<uint2 *>(p) = c; }
+    __device__ static void unpack(const Chunk &c, float (&f)[8]) { unpack8_e4m3(c, f); }
+    // Quantise: code = e4m3(fl32(x / scale)), round to nearest even, saturating.
+    __device__ static Chunk from_bf16(const uint4 &w, float scale) { return quantize8_e4m3(w, scale); }
+};
+
 // Merge (m2, l2, a2) into (m, l, a); an empty state has m = -inf, l = 0, a = 0.
 template <int N>
 __device__ __forceinline__ void merge_state(float &m, float &l, float (&a)[N], float m2, float l2,
@@ -59,40 +86,174 @@ __device__ __forceinline__ void merge_state(float &m, float &l, float (&a)[N], f
     m = mm;
 }
 
+// Lazy rescaling: the running reference m only moves when a score exceeds it
+// by more than this (log2 units), so weights stay below 2^8 and the
+// accumulator is rescaled rarely instead of on every tile.  Any reference
+// gives the same softmax: states carry (m, l, acc) relative to their own m.
+constexpr float kRescaleSlack = 8.0f;
+
 // One lane group's online-softmax update with a 16-key tile: this lane holds
-// dims 8*sub..8*sub+7 of keys t+grp, t+grp+4, t+grp+8, t+grp+12.
-__device__ __forceinline__ void consume_tile(const uint4 (&kw)[4], const uint4 (&vw)[4], const float (&qf)[8], int t,
-                                             int grp, int key1, float &m, float &l, float (&acc)[8]) {
+// dims 8*sub..8*sub+7 of keys t+grp, t+grp+4, t+grp+8, t+grp+12.  kFull: every
+// key of the tile is valid (no masking).
+template <typename KV, bool kFull>
+__device__ __forceinline__ void consume_tile(const typename KV::Chunk (&kw)[4], const typename KV::Chunk (&vw)[4],
+                                             const float (&qf)[8], int t, int grp, int key1, float &m, float &l,
+                                             float (&acc)[8]) {
     float sc[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         float kf[8];
-        unpack8(kw[u], kf);
+        KV::unpack(kw[u], kf);
         float d = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) d = fmaf(qf[j], kf[j], d);
         d += __shfl_xor_sync(0xFFFFFFFFu, d, 1);
         d += __shfl_xor_sync(0xFFFFFFFFu, d, 2);
         d += __shfl_xor_sync(0xFFFFFFFFu, d, 4);
-        sc[u] = (t + grp + 4 * u < key1) ? d : -INFINITY;
+        sc[u] = (kFull || t + grp + 4 * u < key1) ? d : -INFINITY;
     }
     const float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-    const float mn = fmaxf(m, mt);
-    if (mn == -INFINITY) return;   // this lane group had no valid key yet
-    const float corr = exp2f(m - mn);
-    l *= corr;
+    if (mt > m + kRescaleSlack) {   // also taken for the first valid key (m = -inf)
+        const float corr = fast_exp2(m - mt);
+        l *= corr;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] *= corr;
+        for (int j = 0; j < 8; ++j) acc[j] *= corr;
+        m = mt;
+    }
+    if (m == -INFINITY) return;   // this lane group had no valid key yet
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        const float pu = exp2f(sc[u] - mn);
+        const float pu = fast_exp2(sc[u] - m);
         l += pu;
         float vf[8];
-        unpack8(vw[u], vf);
+        KV::unpack(vw[u], vf);
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = fmaf(pu, vf[j], acc[j]);
     }
-    m = mn;
+}
+
+// Which rows an attend_range body serves.
+enum RowKind { kSelfRows, kCrossRows, kEitherRows };
+
+// Stream this CTA's tiles [key0, key1) of row (b, h) through the online softmax
+// (warp w takes tiles w, w+4, ...).  kKind selects the self rows, the
+// description-encoder rows of a fused launch (contiguous bf16), or either at
+// run time (one loop body for both when the self cache is bf16 too, which
+// keeps the fused kernel within 64 registers).  kPipelined keeps the next
+// tile's loads in flight while the current one is consumed.  Launch
+// parameters are read from the parameter space, not copied into registers.
+template <typename KV, bool kPaged, bool kPipelined, bool kAppend, RowKind kKind>
+__device__ __forceinline__ void attend_range(const AttnParams &p, bool cross_row, int b, int h, int key0, int key1,
+                                             int newpos, const float (&qf)[8], int warp, int lane, float &m, float &l,
+                                             float (&acc)[8]) {
+    using Chunk = typename KV::Chunk;
+    constexpr size_t kRowBytes = (size_t)kD * KV::kElemBytes;
+    const int grp = lane >> 3, sub = lane & 7;
+    const size_t row = (size_t)b * p.H + h;
+    const bool cross = kKind == kCrossRows || (kKind == kEitherRows && cross_row);
+    const bool paged = kPaged && !cross;
+    const uint8_t *kc = reinterpret_cast<const uint8_t *>(cross ? p.xk : p.k);
+    const uint8_t *vc = reinterpret_cast<const uint8_t *>(cross ? p.xv : p.v);
+
+    // Issue the loads of tile t (zeros past key1 or for an unmapped block).  With
+    // kAppend, the key at newpos is this step's k_new/v_new, converted to the
+    // cache format, stored into its cache slot and used from registers.
+    auto load_tile = [&](int t, Chunk (&kw)[4], Chunk (&vw)[4]) -> bool {
+        size_t base = 0;
+        bool ok = true;
+        if (paged) {
+            const int blk = __ldg(p.table + (size_t)b * p.max_blocks + t / kTile);
+            ok = (unsigned)blk < (unsigned)p.num_blocks;
+            base = ok ? ((size_t)blk * p.H + h) * (size_t)kTile * kRowBytes : 0;
+        } else {
+            base = (row * (size_t)(cross ? p.xcap : p.cap) + (size_t)t) * kRowBytes;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int rr = grp + 4 * u;
+            const size_t off = base + (size_t)rr * kRowBytes + (size_t)sub * 8 * KV::kElemBytes;
+            if (ok && t + rr < key1) {
+                if (kAppend && t + rr == newpos) {
+                    kw[u] = KV::from_bf16(ld_ro16(p.k_new + row * kD + sub * 8), p.k_scale);
+                    vw[u] = KV::from_bf16(ld_ro16(p.v_new + row * kD + sub * 8), p.v_scale);
+                    KV::store(const_cast<uint8_t *>(kc) + off, kw[u]);
+                    KV::store(const_cast<uint8_t *>(vc) + off, vw[u]);
+                } else {
+                    kw[u] = KV::load(kc + off);
+                    vw[u] = KV::load(vc + off);
+                }
+            } else {
+                kw[u] = KV::zero();
+                vw[u] = KV::zero();
+            }
+        }
+        if (kAppend && !ok && t <= newpos && newpos < t + kTile && lane == 0) flag_error(p.err, DR_ERRF_POS);
+        return ok;
+    };
+
+    // Whole tiles away from the appended key need no per-key checks.
+    auto full_tile = [&](int t) -> bool {
+        return t + kTile <= key1 && !(kAppend && newpos >= t && newpos < t + kTile);
+    };
+    auto load_full = [&](int t, Chunk (&kw)[4], Chunk (&vw)[4]) -> bool {
+        size_t base = 0;
+        bool ok = true;
+        if (paged) {
+            const int blk = __ldg(p.table + (size_t)b * p.max_blocks + t / kTile);
+            ok = (unsigned)blk < (unsigned)p.num_blocks;
+            base = ok ? ((size_t)blk * p.H + h) * (size_t)kTile * kRowBytes : 0;
+        } else {
+            base = (row * (size_t)(cross ? p.xcap : p.cap) + (size_t)t) * kRowBytes;
+        }
+        if (ok) {
+            const uint8_t *kp = kc + base + (size_t)grp * kRowBytes + (size_t)sub * 8 * KV::kElemBytes;
+            const uint8_t *vp = vc + base + (size_t)grp * kRowBytes + (size_t)sub * 8 * KV::kElemBytes;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                kw[u] = KV::load(kp + 4 * u * kRowBytes);
+                vw[u] = KV::load(vp + 4 * u * kRowBytes);
+            }
+        }
+        return ok;
+    };
+
+    if constexpr (kPipelined) {
+        Chunk kw[4], vw[4];
+        int t = key0 + warp * kTile;
+        bool full = t < key1 && full_tile(t);
+        bool ok = t < key1 ? (full ? load_full(t, kw, vw) : load_tile(t, kw, vw)) : true;
+        for (; t < key1; t += kWarps * kTile) {
+            Chunk nk[4] = {}, nv[4] = {};
+            const int tn = t + kWarps * kTile;
+            const bool nfull = tn < key1 && full_tile(tn);
+            const bool nok = tn < key1 ? (nfull ? load_full(tn, nk, nv) : load_tile(tn, nk, nv)) : true;
+            if (!ok) {
+                if (lane == 0) flag_error(p.err, DR_ERRF_BLOCK_ID);   // warp-uniform: the tile is skipped
+            } else if (full) {
+                consume_tile<KV, true>(kw, vw, qf, t, grp, key1, m, l, acc);
+            } else {
+                consume_tile<KV, false>(kw, vw, qf, t, grp, key1, m, l, acc);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                kw[u] = nk[u];
+                vw[u] = nv[u];
+            }
+            ok = nok;
+            full = nfull;
+        }
+    } else {
+        for (int t = key0 + warp * kTile; t < key1; t += kWarps * kTile) {
+            Chunk kw[4], vw[4];
+            if (full_tile(t)) {
+                if (load_full(t, kw, vw)) consume_tile<KV, true>(kw, vw, qf, t, grp, key1, m, l, acc);
+                else if (lane == 0) flag_error(p.err, DR_ERRF_BLOCK_ID);
+            } else {
+                if (load_tile(t, kw, vw)) consume_tile<KV, false>(kw, vw, qf, t, grp, key1, m, l, acc);
+                else if (lane == 0) flag_error(p.err, DR_ERRF_BLOCK_ID);
+            }
+        }
+    }
 }
 
 // kPipelined: each warp keeps the next tile's loads in flight while it
@@ -100,7 +261,7 @@ __device__ __forceinline__ void consume_tile(const uint4 (&kw)[4], const uint4 (
 // registers instead of 64).  Chosen when the whole grid is resident at once,
 // i.e. when occupancy is not what limits the bytes in flight.  Both variants
 // perform the same arithmetic in the same order.
-template <bool kPaged, bool kPipelined, bool kFused>
+template <typename KV, bool kPaged, bool kPipelined, bool kFused>
 __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kernel(const AttnParams p) {
     __shared__ float s_wm[kWarps], s_wl[kWarps];
     __shared__ float s_wacc[kWarps][kD];
@@ -117,17 +278,13 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     const int b = !cross ? (int)blockIdx.z
                          : packed ? ((int)blockIdx.z - p.B) * (int)gridDim.x + (int)blockIdx.x : (int)blockIdx.z - p.B;
     if (b >= p.B) return;   // tail of the packed region (no cluster barrier is reached there)
-    const bool paged = kPaged && !cross;
-    const uint16_t *qsrc = cross ? p.xq : p.q;
-    const uint16_t *kcache = cross ? p.xk : p.k;
-    const uint16_t *vcache = cross ? p.xv : p.v;
-    const int cap = cross ? p.xcap : p.cap;
-    void *outp = cross ? p.xout : p.out;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int grp = lane >> 3;   // which key of each group of 4
-    const int sub = lane & 7;    // which 8 dims
+    const int grp = lane >> 3;
+    const int sub = lane & 7;
 
+    const size_t row = (size_t)b * p.H + h;
+    const int cap = cross ? p.xcap : p.cap;
     int L = __ldg((cross ? p.xlens : p.lens) + b);
     // Fused append: this step's key goes to slot L-1 (only for a valid length).
     int newpos = -1;
@@ -144,81 +301,33 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     const int key0 = min(split * per, ntiles) * kTile;
     const int key1 = min(key0 + per * kTile, L);
 
-    const size_t row = (size_t)b * p.H + h;
     float qf[8];
-    unpack8(ld_ro16(qsrc + row * kD + sub * 8), qf);
+    unpack8(ld_ro16((cross ? p.xq : p.q) + row * kD + sub * 8), qf);
+    const float qscale = cross ? p.xqscale : p.qscale;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) qf[j] *= p.qscale;
+    for (int j = 0; j < 8; ++j) qf[j] *= qscale;
 
     float m = -INFINITY, l = 0.f;
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 
-    // Issue the 16-byte loads of tile t (zeros past key1 or for an unmapped block).
-    // Fused: the key at newpos is this step's k_new/v_new, taken from the inputs
-    // and stored into its cache slot by the same lanes.
-    auto load_tile = [&](int t, uint4 (&kw)[4], uint4 (&vw)[4]) -> bool {
-        const uint16_t *kt;
-        const uint16_t *vt;
-        bool ok = true;
-        if (paged) {
-            const int blk = __ldg(p.table + (size_t)b * p.max_blocks + t / kTile);
-            ok = (unsigned)blk < (unsigned)p.num_blocks;
-            const size_t off = ok ? ((size_t)blk * p.H + h) * (size_t)(kTile * kD) : 0;
-            kt = kcache + off;
-            vt = vcache + off;
-        } else {
-            const size_t off = (row * (size_t)cap + (size_t)t) * kD;
-            kt = kcache + off;
-            vt = vcache + off;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int r = grp + 4 * u;
-            if (ok && t + r < key1) {
-                if (kFused && t + r == newpos) {
-                    kw[u] = ld_ro16(p.k_new + row * kD + sub * 8);
-                    vw[u] = ld_ro16(p.v_new + row * kD + sub * 8);
-                    *reinterpret_cast<uint4 *>(const_cast<uint16_t *>(kt) + r * kD + sub * 8) = kw[u];
-                    *reinterpret_cast<uint4 *>(const_cast<uint16_t *>(vt) + r * kD + sub * 8) = vw[u];
-                } else {
-                    kw[u] = ld_stream16(kt + r * kD + sub * 8);
-                    vw[u] = ld_stream16(vt + r * kD + sub * 8);
-                }
-            } else {
-                kw[u] = make_uint4(0, 0, 0, 0);
-                vw[u] = make_uint4(0, 0, 0, 0);
-            }
-        }
-        if (kFused && !ok && t <= newpos && newpos < t + kTile && lane == 0) flag_error(p.err, DR_ERRF_POS);
-        return ok;
-    };
-
-    if constexpr (kPipelined) {
-        uint4 kw[4], vw[4];
-        int t = key0 + warp * kTile;
-        bool ok = t < key1 ? load_tile(t, kw, vw) : true;
-        for (; t < key1; t += kWarps * kTile) {
-            uint4 nk[4] = {}, nv[4] = {};
-            const int tn = t + kWarps * kTile;
-            const bool nok = tn < key1 ? load_tile(tn, nk, nv) : true;
-            if (ok) consume_tile(kw, vw, qf, t, grp, key1, m, l, acc);
-            else if (lane == 0) flag_error(p.err, DR_ERRF_BLOCK_ID);   // warp-uniform: the tile is skipped
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                kw[u] = nk[u];
-                vw[u] = nv[u];
-            }
-            ok = nok;
-        }
+    if constexpr (kFused && std::is_same<KV, Bf16Kv>::value) {
+        attend_range<KV, kPaged, kPipelined, true, kEitherRows>(p, cross, b, h, key0, key1, newpos, qf, warp, lane, m,
+                                                                 l, acc);
+    } else if constexpr (kFused) {
+        if (cross)
+            attend_range<Bf16Kv, false, kPipelined, false, kCrossRows>(p, true, b, h, key0, key1, -1, qf, warp, lane, m,
+                                                                      l, acc);
+        else
+            attend_range<KV, kPaged, kPipelined, true, kSelfRows>(p, false, b, h, key0, key1, newpos, qf, warp, lane, m,
+                                                                 l, acc);
     } else {
-        for (int t = key0 + warp * kTile; t < key1; t += kWarps * kTile) {
-            uint4 kw[4], vw[4];
-            if (load_tile(t, kw, vw)) consume_tile(kw, vw, qf, t, grp, key1, m, l, acc);
-            else if (lane == 0) flag_error(p.err, DR_ERRF_BLOCK_ID);   // warp-uniform: the tile is skipped
-        }
+        attend_range<KV, kPaged, kPipelined, false, kSelfRows>(p, false, b, h, key0, key1, -1, qf, warp, lane, m, l,
+                                                              acc);
     }
+    // an e4m3 value is code * v_scale: the kernel accumulates codes and scales the result
+    const float out_scale = cross ? 1.0f : p.out_scale;
 
     // Lanes sub, sub+8, sub+16, sub+24 hold the same dims for different keys.
 #pragma unroll
@@ -260,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
         }
     }
 
+    void *outp = cross ? p.xout : p.out;
     float *out_f = reinterpret_cast<float *>(outp) + row * kD;
     uint16_t *out_h = reinterpret_cast<uint16_t *>(outp) + row * kD;
 
@@ -267,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
         __syncthreads();
         if (threadIdx.x < kD) {
             const int d = threadIdx.x;
-            const float o = s_part.l > 0.f ? s_part.acc[d] / s_part.l : 0.f;
+            const float o = s_part.l > 0.f ? s_part.acc[d] / s_part.l * out_scale : 0.f;
             if (p.out_f32) out_f[d] = o;
             else out_h[d] = f32_to_bf16_rn(o);
         }
@@ -293,14 +403,14 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
                 o += wt * pr->acc[d];
             }
         }
-        o = ls > 0.f ? o / ls : 0.f;
+        o = ls > 0.f ? o / ls * out_scale : 0.f;
         if (p.out_f32) out_f[d] = o;
         else out_h[d] = f32_to_bf16_rn(o);
     }
     cluster.sync();   // keep every CTA's shared memory alive until rank 0 has read it
 }
 
-template <bool kPaged, bool kPipelined, bool kFused>
+template <typename KV, bool kPaged, bool kPipelined, bool kFused>
 cudaError_t launch_variant(const AttnParams &p, int splits, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     unsigned zrows = (unsigned)p.B;
@@ -316,7 +426,7 @@ cudaError_t launch_variant(const AttnParams &p, int splits, cudaStream_t stream)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = splits > 1 ? 1 : 0;
-    auto kern = decode_attn_kernel<kPaged, kPipelined, kFused>;
+    auto kern = decode_attn_kernel<KV, kPaged, kPipelined, kFused>;
     if (splits > 8) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
@@ -327,23 +437,27 @@ cudaError_t launch_variant(const AttnParams &p, int splits, cudaStream_t stream)
 // CTAs of the pipelined kernel that fit on one SM at once (up to 112 registers x 128 threads).
 constexpr int kPipelinedCtasPerSm = 4;
 
-template <bool kFused>
+template <typename KV, bool kFused>
 cudaError_t launch_layout(const AttnParams &p, bool paged, int splits, cudaStream_t stream) {
     long long ctas = (long long)splits * p.H * p.B;
     if (kFused && p.xq) ctas += (long long)p.H * (p.xpacked ? p.B : (long long)splits * p.B);
     const bool pipelined = ctas <= (long long)kPipelinedCtasPerSm * current_device_sms();
     if (paged)
-        return pipelined ? launch_variant<true, true, kFused>(p, splits, stream)
-                         : launch_variant<true, false, kFused>(p, splits, stream);
-    return pipelined ? launch_variant<false, true, kFused>(p, splits, stream)
-                     : launch_variant<false, false, kFused>(p, splits, stream);
+        return pipelined ? launch_variant<KV, true, true, kFused>(p, splits, stream)
+                         : launch_variant<KV, true, false, kFused>(p, splits, stream);
+    return pipelined ? launch_variant<KV, false, true, kFused>(p, splits, stream)
+                     : launch_variant<KV, false, false, kFused>(p, splits, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_attn(const AttnParams &p, bool paged, int splits, cudaStream_t stream) {
     const bool fused = p.k_new != nullptr || p.xq != nullptr;
-    return fused ? launch_layout<true>(p, paged, splits, stream) : launch_layout<false>(p, paged, splits, stream);
+    if (p.kv_fp8)
+        return fused ? launch_layout<Fp8Kv, true>(p, paged, splits, stream)
+                     : launch_layout<Fp8Kv, false>(p, paged, splits, stream);
+    return fused ? launch_layout<Bf16Kv, true>(p, paged, splits, stream)
+                 : launch_layout<Bf16Kv, false>(p, paged, splits, stream);
 }
 
 }  // namespace dr

@@ -38,7 +38,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 dr_status check_cache(const dr_kv_cache *c, int *cap) {
     if (!c || !c->k || !c->v) return DR_ERR_INVALID_ARG;
     if (!aligned16(c->k) || !aligned16(c->v)) return DR_ERR_INVALID_ARG;
-    if (c->reserved != 0) return DR_ERR_INVALID_ARG;
+    if (c->kv_dtype != DR_KV_BF16 && c->kv_dtype != DR_KV_FP8_E4M3) return DR_ERR_INVALID_ARG;
+    if (c->kv_dtype == DR_KV_FP8_E4M3) {
+        if (!(c->k_scale > 0.f) || !(c->v_scale > 0.f) || isinf(c->k_scale) || isinf(c->v_scale))
+            return DR_ERR_INVALID_ARG;
+        if (!aligned16(c->k) || !aligned16(c->v)) return DR_ERR_INVALID_ARG;
+    }
     if (c->layout == DR_KV_CONTIGUOUS) {
         if (c->max_len < 1) return DR_ERR_INVALID_ARG;
         *cap = c->max_len;
@@ -69,11 +74,11 @@ float softmax_scale_log2(float scale, int D) {
 
 void fill_self(dr::AttnParams &p, const void *q, const void *k, const void *v, const int32_t *lens,
                const int32_t *table, int B, int H, int cap, int max_blocks, int num_blocks, float scale, void *out,
-               dr_dtype out_dtype, int32_t *err_flag) {
+               dr_dtype out_dtype, int32_t *err_flag, bool fp8 = false, float k_scale = 1.f, float v_scale = 1.f) {
     p = dr::AttnParams{};
     p.q = static_cast<const uint16_t *>(q);
-    p.k = static_cast<const uint16_t *>(k);
-    p.v = static_cast<const uint16_t *>(v);
+    p.k = k;
+    p.v = v;
     p.lens = lens;
     p.table = table;
     p.B = B;
@@ -81,10 +86,24 @@ void fill_self(dr::AttnParams &p, const void *q, const void *k, const void *v, c
     p.cap = cap;
     p.max_blocks = max_blocks;
     p.num_blocks = num_blocks;
-    p.qscale = softmax_scale_log2(scale, dr::kHeadDim);
+    p.kv_fp8 = fp8 ? 1 : 0;
+    p.k_scale = fp8 ? k_scale : 1.f;
+    p.v_scale = fp8 ? v_scale : 1.f;
+    // an e4m3 key is code * k_scale: fold k_scale into the query scale, v_scale into the output
+    p.qscale = softmax_scale_log2(scale, dr::kHeadDim) * p.k_scale;
+    p.out_scale = p.v_scale;
+    p.xqscale = softmax_scale_log2(scale, dr::kHeadDim);
     p.out = out;
     p.out_f32 = out_dtype == DR_F32;
     p.err = err_flag;
+}
+
+void fill_cache(dr::AttnParams &p, const void *q, const dr_kv_cache *c, const int32_t *lens, int B, int H, int cap,
+                float scale, void *out, dr_dtype out_dtype, int32_t *err_flag) {
+    const bool paged = c->layout == DR_KV_PAGED;
+    fill_self(p, q, c->k, c->v, lens, paged ? c->block_table : nullptr, B, H, cap, paged ? c->max_blocks_per_seq : 0,
+              paged ? c->num_blocks : 0, scale, out, out_dtype, err_flag, c->kv_dtype == DR_KV_FP8_E4M3, c->k_scale,
+              c->v_scale);
 }
 
 dr_status check_attn_args(const void *q, const int32_t *lens, void *out, dr_dtype out_dtype, float scale) {
@@ -131,8 +150,11 @@ dr_status dr_kv_append(const dr_kv_cache *cache, const void *k_new, const void *
     if (st != DR_OK) return st;
     if (!k_new || !v_new || !pos || !aligned16(k_new) || !aligned16(v_new)) return DR_ERR_INVALID_ARG;
     dr::AppendParams p;
-    p.k = static_cast<uint16_t *>(cache->k);
-    p.v = static_cast<uint16_t *>(cache->v);
+    p.k = cache->k;
+    p.v = cache->v;
+    p.kv_fp8 = cache->kv_dtype == DR_KV_FP8_E4M3;
+    p.k_scale = cache->k_scale;
+    p.v_scale = cache->v_scale;
     p.k_new = static_cast<const uint16_t *>(k_new);
     p.v_new = static_cast<const uint16_t *>(v_new);
     p.pos = pos;
@@ -156,11 +178,9 @@ dr_status dr_decode_self_attn(const void *q, const dr_kv_cache *cache, const int
     if (st != DR_OK) return st;
     st = check_attn_args(q, seq_len, out, out_dtype, scale);
     if (st != DR_OK) return st;
-    const bool paged = cache->layout == DR_KV_PAGED;
     dr::AttnParams p;
-    fill_self(p, q, cache->k, cache->v, seq_len, paged ? cache->block_table : nullptr, B, H, cap,
-              paged ? cache->max_blocks_per_seq : 0, paged ? cache->num_blocks : 0, scale, out, out_dtype, err_flag);
-    return launch(p, paged, max_seq_len_hint, stream);
+    fill_cache(p, q, cache, seq_len, B, H, cap, scale, out, out_dtype, err_flag);
+    return launch(p, cache->layout == DR_KV_PAGED, max_seq_len_hint, stream);
 }
 
 dr_status dr_decode_cross_attn(const void *q, const void *k_enc, const void *v_enc, const int32_t *enc_len, int B,
@@ -193,8 +213,7 @@ dr_status dr_decode_layer(const void *q, const dr_kv_cache *cache, const void *k
     if (!aligned16(q_cross) || !aligned16(k_enc) || !aligned16(v_enc)) return DR_ERR_INVALID_ARG;
     const bool paged = cache->layout == DR_KV_PAGED;
     dr::AttnParams p;
-    fill_self(p, q, cache->k, cache->v, seq_len, paged ? cache->block_table : nullptr, B, H, cap,
-              paged ? cache->max_blocks_per_seq : 0, paged ? cache->num_blocks : 0, scale, out, out_dtype, err_flag);
+    fill_cache(p, q, cache, seq_len, B, H, cap, scale, out, out_dtype, err_flag);
     p.k_new = static_cast<const uint16_t *>(k_new);
     p.v_new = static_cast<const uint16_t *>(v_new);
     p.xq = static_cast<const uint16_t *>(q_cross);

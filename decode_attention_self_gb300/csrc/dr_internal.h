@@ -23,21 +23,24 @@ int current_device_sms();
 
 struct AttnParams {
     const uint16_t *q;       // [B][H][64] bf16 bits
-    const uint16_t *k;       // contiguous [B][H][cap][64] or paged [NB][H][16][64]
-    const uint16_t *v;
+    const void *k;           // contiguous [B][H][cap][64] or paged [NB][H][16][64], bf16 or e4m3
+    const void *v;
     const int32_t *lens;     // [B]
     const int32_t *table;    // paged: [B][max_blocks]
     int32_t B, H;
     int32_t cap;             // keys a row can hold
     int32_t max_blocks;      // paged: block-table row stride
     int32_t num_blocks;      // paged: pool size
-    float qscale;            // softmax scale * log2(e)
+    int32_t kv_fp8;          // 1: the cache holds e4m3 codes (k = code * k_scale, v = code * v_scale)
+    float qscale;            // softmax scale * log2(e) (* k_scale for an e4m3 cache)
+    float k_scale, v_scale;  // e4m3 cache scales (used by the fused append)
+    float out_scale;         // v_scale for an e4m3 cache, else 1
     void *out;               // [B][H][64]
     int32_t out_f32;
     int32_t *err;
     // Fused decode-layer launch only (see dr_decode_layer): this step's key and
     // value, stored at position lens[b]-1 of the cache and used from registers,
-    // and a second set of B rows attending the description encoder's keys.
+    // and a second set of B rows attending the description encoder's keys (bf16).
     const uint16_t *k_new;   // [B][H][64] or null
     const uint16_t *v_new;
     const uint16_t *xq;      // cross rows: [B][H][64] or null (no cross rows)
@@ -45,6 +48,7 @@ struct AttnParams {
     const uint16_t *xv;
     const int32_t *xlens;    // [B]
     int32_t xcap;
+    float xqscale;           // softmax scale * log2(e) for the cross rows
     void *xout;              // [B][H][64]
     int32_t xpacked;         // 1: one CTA per cross row, gridDim.x rows per cluster; 0: rows split like self rows
 };
@@ -52,11 +56,13 @@ struct AttnParams {
 cudaError_t launch_decode_attn(const AttnParams &p, bool paged, int splits, cudaStream_t stream);
 
 struct AppendParams {
-    uint16_t *k, *v;
+    void *k, *v;                     // bf16 or e4m3 cache
     const uint16_t *k_new, *v_new;   // [B][H][64]
     const int32_t *pos;              // [B]
     const int32_t *table;            // paged only
     int32_t B, H, cap, max_blocks, num_blocks;
+    int32_t kv_fp8;                  // quantise to e4m3: code = e4m3(fl32(x / scale))
+    float k_scale, v_scale;
     int32_t *err;
 };
 

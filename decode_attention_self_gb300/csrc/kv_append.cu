@@ -4,9 +4,9 @@
 // for causal attention, preallocated so that the decode step can be captured
 // as one CUDA graph; and "Future work" item 1, the paged alternative.
 //
-// One thread moves 16 bytes (8 bf16) of k and of v: B*H*8 threads.  The
-// write position comes from device memory, so the same launch (or captured
-// graph) serves every step.
+// One thread moves 8 elements of k and of v (16 bytes of bf16, or 8 e4m3 codes
+// quantised from them): B*H*8 threads.  The write position comes from device
+// memory, so the same launch (or captured graph) serves every step.
 #include "dr_device.cuh"
 #include "dr_internal.h"
 
@@ -15,7 +15,7 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <bool kPaged>
+template <bool kPaged, bool kFp8>
 __global__ void __launch_bounds__(kThreads) kv_append_kernel(const AppendParams p) {
     const long long idx = (long long)blockIdx.x * kThreads + threadIdx.x;
     const long long total = (long long)p.B * p.H * 8;
@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const AppendParams 
         if (h == 0 && chunk == 0) flag_error(p.err, DR_ERRF_POS);
         return;
     }
-    size_t dst;
+    size_t dst;   // element offset of the row's slot
     if constexpr (kPaged) {
         const int blk = __ldg(p.table + (size_t)b * p.max_blocks + pos / kBlockKeys);
         if ((unsigned)blk >= (unsigned)p.num_blocks) {
@@ -43,8 +43,15 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const AppendParams 
     const size_t src = (size_t)row * kHeadDim + chunk * 8;
     const uint4 kn = ld_ro16(p.k_new + src);
     const uint4 vn = ld_ro16(p.v_new + src);
-    *reinterpret_cast<uint4 *>(p.k + dst + chunk * 8) = kn;
-    *reinterpret_cast<uint4 *>(p.v + dst + chunk * 8) = vn;
+    if constexpr (kFp8) {
+        uint8_t *k = static_cast<uint8_t *>(p.k), *v = static_cast<uint8_t *>(p.v);
+        *reinterpret_cast<uint2 *>(k + dst + chunk * 8) = quantize8_e4m3(kn, p.k_scale);
+        *reinterpret_cast<uint2 *>(v + dst + chunk * 8) = quantize8_e4m3(vn, p.v_scale);
+    } else {
+        uint16_t *k = static_cast<uint16_t *>(p.k), *v = static_cast<uint16_t *>(p.v);
+        *reinterpret_cast<uint4 *>(k + dst + chunk * 8) = kn;
+        *reinterpret_cast<uint4 *>(v + dst + chunk * 8) = vn;
+    }
 }
 
 }  // namespace
@@ -52,8 +59,13 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const AppendParams 
 cudaError_t launch_kv_append(const AppendParams &p, bool paged, cudaStream_t stream) {
     const long long total = (long long)p.B * p.H * 8;
     const unsigned grid = (unsigned)((total + kThreads - 1) / kThreads);
-    if (paged) kv_append_kernel<true><<<grid, kThreads, 0, stream>>>(p);
-    else kv_append_kernel<false><<<grid, kThreads, 0, stream>>>(p);
+    if (p.kv_fp8) {
+        if (paged) kv_append_kernel<true, true><<<grid, kThreads, 0, stream>>>(p);
+        else kv_append_kernel<false, true><<<grid, kThreads, 0, stream>>>(p);
+    } else {
+        if (paged) kv_append_kernel<true, false><<<grid, kThreads, 0, stream>>>(p);
+        else kv_append_kernel<false, false><<<grid, kThreads, 0, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 

@@ -135,11 +135,35 @@ def bits(t: torch.Tensor) -> np.ndarray:
 @dataclasses.dataclass
 class SelfCache:
     layout: str
-    k: torch.Tensor             # contiguous [B,H,cap,D] or paged [NB,H,16,D], bf16
+    k: torch.Tensor             # contiguous [B,H,cap,D] or paged [NB,H,16,D]; bf16, or uint8 e4m3 codes
     v: torch.Tensor
     cap: int
     block_table: torch.Tensor | None = None   # [B, max_blocks] int32
     num_blocks: int = 0
+    k_scale: float = 1.0        # e4m3 caches: key = code * k_scale
+    v_scale: float = 1.0
+
+
+E4M3_NAN_CODE = 0x7F
+FP8_SCALE = 1.0 / 64.0
+
+
+def to_e4m3_codes(t: torch.Tensor, scale: float, invalid: torch.Tensor | None = None) -> torch.Tensor:
+    """Seeded e4m3 codes for a synthetic fp8 cache: torch's own float8 conversion of t / scale
+    (clamped to the format's +-448), as uint8; `invalid` slots get the NaN code 0x7F."""
+    codes = (t.float() / scale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    if invalid is not None:
+        codes = codes.masked_fill(invalid, E4M3_NAN_CODE)
+    return codes
+
+
+def make_self_cache_fp8(w: Workload, layer: int, device="cpu", filled_len: np.ndarray | None = None,
+                        k_scale: float = FP8_SCALE, v_scale: float = FP8_SCALE) -> SelfCache:
+    """The bf16 cache of make_self_cache, held as e4m3 codes (NaN code past the valid keys)."""
+    c = make_self_cache(w, layer, device, filled_len)
+    k = to_e4m3_codes(torch.nan_to_num(c.k.float(), nan=0.0), k_scale, torch.isnan(c.k))
+    v = to_e4m3_codes(torch.nan_to_num(c.v.float(), nan=0.0), v_scale, torch.isnan(c.v))
+    return SelfCache(c.layout, k, v, c.cap, c.block_table, c.num_blocks, k_scale, v_scale)
 
 
 def make_block_table(w: Workload, device="cpu", key: int = 0):
@@ -235,5 +259,5 @@ def ceil_div(a: int, b: int) -> int:
     return -(-a // b)
 
 
-__all__ = ["Workload", "make_workload", "make_self_cache", "make_step_inputs", "make_cross_kv", "make_logits",
+__all__ = ["Workload", "make_workload", "make_self_cache", "make_self_cache_fp8", "to_e4m3_codes", "make_step_inputs", "make_cross_kv", "make_logits",
            "make_block_table", "bits", "randn_bf16", "SelfCache", "BLOCK", "BF16_NAN_BITS", "ceil_div"]

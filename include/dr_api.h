@@ -60,6 +60,12 @@ typedef enum dr_kv_layout {
 
 typedef enum dr_dtype { DR_BF16 = 0, DR_F32 = 1 } dr_dtype;
 
+/* Storage format of a self-attention KV cache. */
+typedef enum dr_kv_dtype {
+    DR_KV_BF16 = 0,    /* bf16 keys and values */
+    DR_KV_FP8_E4M3 = 1 /* OCP FP8 E4M3 codes: key = code * k_scale, value = code * v_scale */
+} dr_kv_dtype;
+
 /* Device-side error bits (see err_flag above). */
 #define DR_ERRF_SEQ_LEN 1  /* a seq_len / enc_len entry outside [1, capacity]; it was clamped */
 #define DR_ERRF_BLOCK_ID 2 /* a needed block-table entry outside [0, num_blocks); its keys were skipped */
@@ -75,15 +81,20 @@ typedef enum dr_dtype { DR_BF16 = 0, DR_F32 = 1 } dr_dtype;
  * Static cache (Optimized Parler TTS, "Analysis and improvements": the static
  * caches for causal and cross attention that CUDA-graph capture needs,
  * preallocated to a maximum length):
- *   layout = DR_KV_CONTIGUOUS; k, v = [B][H][max_len][D] bf16; key j of row
+ *   layout = DR_KV_CONTIGUOUS; k, v = [B][H][max_len][D]; key j of row
  *   (b, h) at ((b*H + h)*max_len + j)*D.  Capacity = max_len keys per row.
  * Paged cache (same page, "Future work" item 1: a PagedAttention-style cache
  * so that no full static cache has to be kept or moved):
- *   layout = DR_KV_PAGED; k, v = [num_blocks][H][block_size][D] bf16;
+ *   layout = DR_KV_PAGED; k, v = [num_blocks][H][block_size][D];
  *   block_table = [B][max_blocks_per_seq] int32; key j of row b lives in block
  *   block_table[b][j / block_size], slot j % block_size; entries a row does
  *   not use may hold any value (conventionally -1).  block_size must be 16.
  *   Capacity = max_blocks_per_seq * block_size keys per row.
+ * Element format (kv_dtype): bf16, or FP8 E4M3 codes (the same page's
+ * "Future work" item 1 asks for less KV traffic; 8-bit codes halve it).  An
+ * e4m3 cache stores code = e4m3(fl32(x / scale)) (IEEE division, round to
+ * nearest even, saturating at +-448) and is read back as code * scale, with
+ * k_scale for keys and v_scale for values (both > 0; ignored for bf16).
  * k and v must be 16-byte aligned.  The struct itself is read on the host
  * during the call only.
  */
@@ -93,10 +104,12 @@ typedef struct dr_kv_cache {
     int32_t block_size;         /* paged: keys per block (16); ignored when contiguous */
     int32_t num_blocks;         /* paged: blocks in the pool */
     int32_t max_blocks_per_seq; /* paged: row stride of block_table */
-    int32_t reserved;           /* must be 0 */
-    void *k;                    /* bf16 keys (device) */
-    void *v;                    /* bf16 values (device) */
+    int32_t kv_dtype;           /* dr_kv_dtype */
+    void *k;                    /* keys (device) */
+    void *v;                    /* values (device) */
     const int32_t *block_table; /* paged: [B][max_blocks_per_seq] int32 (device); NULL when contiguous */
+    float k_scale;              /* e4m3 only: key = code * k_scale */
+    float v_scale;              /* e4m3 only: value = code * v_scale */
 } dr_kv_cache;
 
 /*
@@ -104,14 +117,15 @@ typedef struct dr_kv_cache {
  * Source: Optimized Parler TTS, "Analysis and improvements" (static cache
  * for causal attention; each decode step adds one key/value per row).
  *
- *   k_new, v_new : [B][H][D] bf16 (device, 16-byte aligned)
+ *   k_new, v_new : [B][H][D] bf16 (device, 16-byte aligned); quantised to
+ *                  e4m3 codes when the cache is DR_KV_FP8_E4M3
  *   pos          : [B] int32 (device); row b's key/value go to position pos[b]
  *                  (the row's valid length becomes pos[b] + 1 for the
  *                  self-attention that follows)
  *   err_flag     : nullable device int32; DR_ERRF_POS is ORed in when
  *                  pos[b] is outside [0, capacity) or, paged, its block-table
  *                  entry is outside the pool; that row is not written.
- * Writes exactly B*H*D*2 bytes into each of cache->k and cache->v.
+ * Writes exactly B*H*D elements into each of cache->k and cache->v.
  */
 dr_status dr_kv_append(const dr_kv_cache *cache, const void *k_new, const void *v_new, const int32_t *pos, int B,
                        int H, int D, int32_t *err_flag, void *stream);

@@ -52,8 +52,9 @@ def test_status_strings(lib):
 
 class Cache(ctypes.Structure):
     _fields_ = [("layout", ctypes.c_int32), ("max_len", ctypes.c_int32), ("block_size", ctypes.c_int32),
-                ("num_blocks", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("block_table", ctypes.c_void_p)]
+                ("num_blocks", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+                ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 FAKE = 0x10000   # a 16-byte aligned non-null address; never dereferenced on the host
@@ -80,11 +81,15 @@ def test_host_validation_rejects_before_any_launch(lib):
     cpn = Cache(1, 0, 16, 10, 4, 0, FAKE, FAKE, None)
     assert lib.dr_decode_self_attn(vp(FAKE), ctypes.byref(cpn), vp(FAKE), 1, 16, 64, 0, ctypes.c_float(0), vp(FAKE),
                                    0, None, None) == 1
-    # unknown layout, nonzero reserved field
+    # unknown layout, unknown KV format, e4m3 cache without positive scales
     assert lib.dr_decode_self_attn(vp(FAKE), ctypes.byref(Cache(7, 16, 0, 0, 0, 0, FAKE, FAKE, None)), vp(FAKE), 1,
                                    16, 64, 0, ctypes.c_float(0), vp(FAKE), 0, None, None) == 1
-    assert lib.dr_decode_self_attn(vp(FAKE), ctypes.byref(Cache(0, 16, 0, 0, 0, 1, FAKE, FAKE, None)), vp(FAKE), 1,
+    assert lib.dr_decode_self_attn(vp(FAKE), ctypes.byref(Cache(0, 16, 0, 0, 0, 5, FAKE, FAKE, None)), vp(FAKE), 1,
                                    16, 64, 0, ctypes.c_float(0), vp(FAKE), 0, None, None) == 1
+    assert lib.dr_decode_self_attn(vp(FAKE), ctypes.byref(Cache(0, 16, 0, 0, 0, 1, FAKE, FAKE, None, 0.0, 1.0)),
+                                   vp(FAKE), 1, 16, 64, 0, ctypes.c_float(0), vp(FAKE), 0, None, None) == 1
+    assert lib.dr_kv_append(ctypes.byref(Cache(0, 16, 0, 0, 0, 1, FAKE, FAKE, None, 1.0, float("inf"))), vp(FAKE),
+                            vp(FAKE), vp(FAKE), 1, 16, 64, None, None) == 1
     # cross attention: Lc_max < 1, bad out dtype, NaN scale
     assert lib.dr_decode_cross_attn(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 1, 16, 64, 0, ctypes.c_float(0),
                                     vp(FAKE), 0, None, None) == 1
