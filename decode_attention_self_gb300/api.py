@@ -47,7 +47,7 @@ _lib.dr_decode_layer.argtypes = [_vp, ctypes.POINTER(dr_kv_cache), _vp, _vp, _vp
                                  _i, _f, _vp, _vp, _i, _vp, _vp]
 _lib.dr_sample_topk_delayed.argtypes = [_vp, _i, _i, _i, _i, _f, _i, _vp, _vp, ctypes.c_int32, _vp, _vp, _i, _vp]
 _lib.dr_embed_tokens.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _i, _vp, _vp]
-_lib.dr_lm_head.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]
+_lib.dr_lm_head.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp]
 _lib.dr_plan_splits.argtypes = [_i, _i, _i, _i]
 _lib.dr_plan_splits.restype = _i
 _lib.dr_status_string.argtypes = [_i]
@@ -227,14 +227,16 @@ def dr_embed_tokens(tokens: torch.Tensor, table: torch.Tensor, V: int, out: torc
     return out
 
 
-def dr_lm_head(hidden: torch.Tensor, W: torch.Tensor, C: int, logits: torch.Tensor, stream=None) -> torch.Tensor:
+def dr_lm_head(hidden: torch.Tensor, W: torch.Tensor, C: int, logits: torch.Tensor,
+               err_flag: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """logits [B,C,ldv] float32 from hidden [B,K] bf16 and merged heads W [C*V, K] bf16 (V = W rows / C)."""
     B, K = hidden.shape
     V = W.shape[0] // C
     ldv = logits.shape[2]
     _check("dr_lm_head",
            _lib.dr_lm_head(_ptr(hidden, torch.bfloat16, "hidden"), _ptr(W, torch.bfloat16, "W"), B, K, C, V, ldv,
-                           _ptr(logits, torch.float32, "logits"), _stream(stream)))
+                           _ptr(logits, torch.float32, "logits"), _ptr(err_flag, torch.int32, "err_flag"),
+                           _stream(stream)))
     return logits
 
 

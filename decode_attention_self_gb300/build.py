@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdecoderattn.so")
-SOURCES = ["dr_api.cu", "attention.cu", "kv_append.cu", "sampler.cu", "heads.cu"]
+SOURCES = ["dr_api.cu", "attention.cu", "kv_append.cu", "sampler.cu", "heads.cu", "lm_head_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -275,7 +275,7 @@ dr_status dr_embed_tokens(const int32_t *tokens, const void *table, int B, int C
 }
 
 dr_status dr_lm_head(const void *hidden, const void *W, int B, int K, int C, int V, int ldv, float *logits,
-                     void *stream) {
+                     int32_t *err_flag, void *stream) {
     if (!hidden || !W || !logits || !aligned16(hidden) || !aligned16(W)) return DR_ERR_INVALID_ARG;
     if (B < 1 || C < 1 || V < 1 || ldv < V || K < 1) return DR_ERR_INVALID_ARG;
     if ((long long)C * V > 0x7FFFFFFFLL) return DR_ERR_INVALID_ARG;
@@ -290,6 +290,7 @@ dr_status dr_lm_head(const void *hidden, const void *W, int B, int K, int C, int
     p.C = C;
     p.V = V;
     p.ldv = ldv;
+    p.err = err_flag;
     return from_cuda(dr::launch_lm_head(p, static_cast<cudaStream_t>(stream)));
 }
 

@@ -95,8 +95,13 @@ struct LmHeadParams {
     const uint16_t *W;       // [C*V][K] bf16
     float *logits;           // [B][C][ldv]
     int32_t B, K, C, V, ldv;
+    int32_t *err;
 };
 
 cudaError_t launch_lm_head(const LmHeadParams &p, cudaStream_t stream);
+
+// Batches from this size on run the merged head on the tensor cores (tcgen05).
+constexpr int kLmHeadTensorCoreMinBatch = 16;
+cudaError_t launch_lm_head_tc(const LmHeadParams &p, int32_t *err, cudaStream_t stream);
 
 }  // namespace dr

@@ -10,10 +10,12 @@
 //     codebook heads merged into one weight matrix [C*V][K]), writing fp32
 //     logits straight into the sampler's [B][C][ldv] layout.
 //
-// Both are bound by HBM at decode batch sizes: the embedding gathers C rows of
-// Dm bf16 per batch row; the head streams the C*V x K bf16 weight matrix once
-// per launch and applies every weight row to all B hidden vectors from shared
-// memory (fp32 accumulation on the CUDA cores).
+// The embedding gathers C rows of Dm bf16 per batch row (HBM/launch bound).  At
+// small batch the head is a matrix-vector product bound by streaming the
+// C*V x K bf16 weights once: the CUDA-core kernel here applies every weight row
+// to all B hidden vectors from shared memory (fp32 accumulation).  From
+// kLmHeadTensorCoreMinBatch rows on it is a dense contraction and runs on the
+// tensor cores (lm_head_tc.cu).
 #include "dr_device.cuh"
 #include "dr_internal.h"
 
@@ -154,6 +156,7 @@ cudaError_t launch_embed_tokens(const EmbedParams &p, cudaStream_t stream) {
 }
 
 cudaError_t launch_lm_head(const LmHeadParams &p, cudaStream_t stream) {
+    if (p.B >= kLmHeadTensorCoreMinBatch) return launch_lm_head_tc(p, p.err, stream);
     switch (p.K / 256) {
         case 1: return launch_head<1>(p, stream);
         case 2: return launch_head<2>(p, stream);

@@ -1,0 +1,283 @@
+// Merged LM head on the 5th-generation tensor cores, for decode batches large
+// enough to make the head a dense contraction (Optimized Parler TTS, "Analysis
+// and improvements", other optimizations items 1-2: the head on the last
+// position only, the nine codebook heads merged into one weight matrix).
+//
+//   logits^T[n, b] = sum_k W[n, k] * hidden[b, k]       (n = c*V + v)
+//
+// One CTA computes a 128-row slab of W against a tile of up to 256 batch rows:
+// the weight slab is the MMA's M = 128 operand A, the batch tile its N operand
+// B, both K-major bf16 in shared memory with the 128-byte swizzle, and the fp32
+// accumulator lives in tensor memory (128 lanes x N columns).
+//   warp 0, lane 0 : TMA producer -- cp.async.bulk.tensor.2d loads of 64-wide K
+//                    chunks of A and B into a 4-stage ring, completion counted
+//                    on the stage's "full" mbarrier;
+//   warp 1, lane 0 : MMA issuer -- four tcgen05.mma (K = 16 each) per chunk,
+//                    tcgen05.commit to the stage's "empty" mbarrier, and a last
+//                    commit to "done";
+//   all 4 warps    : epilogue -- warp w reads TMEM lanes 32w..32w+31 with
+//                    tcgen05.ld and writes fp32 logits into the sampler layout.
+// Every wait is bounded: a wait that runs out sets DR_ERRF_TIMEOUT and the CTA
+// skips the rest of its work (a correct launch never gets there).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "dr_device.cuh"
+#include "dr_internal.h"
+
+namespace dr {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kTileN = 128;          // W rows per CTA (MMA M)
+constexpr int kChunkK = 64;          // K elements per stage: one 128-byte swizzled row
+constexpr int kStages = 4;
+constexpr int kMaxBatchTile = 256;   // MMA N limit
+constexpr long long kWaitLimit = 4LL << 30;   // clock cycles (about 2 s)
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Bounded wait for the phase with the given parity; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (true) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (clock64() - t0 > kWaitLimit) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row
+// groups 1024 bytes apart (start address, leading / stride byte offsets >> 4,
+// descriptor version 1, swizzle mode 2 = 128B).
+__device__ __forceinline__ uint64_t smem_desc(const void *p) {
+    const uint64_t addr = smem_u32(p);
+    return ((addr & 0x3FFFFull) >> 4) | (1ull << 16) | ((1024ull >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+            tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+struct TcParams {
+    float *logits;     // [B][C][ldv]
+    int32_t B, K, C, V, ldv, btile, tmem_cols;
+    int32_t *err;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    lm_head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
+                      const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t full[kStages], empty[kStages], done;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kTileN;
+    const int b0 = blockIdx.y * p.btile;
+    const int N = p.C * p.V;
+    const int chunks = p.K / kChunkK;
+    const uint32_t bytes_a = kTileN * kChunkK * 2;
+    const uint32_t bytes_b = (uint32_t)p.btile * kChunkK * 2;
+
+    // 1024-byte aligned stage ring: A stages, then B stages
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sa = base;
+    uint8_t *sb = base + kStages * bytes_a;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&done, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
+                     "r"(p.tmem_cols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // producer
+        for (int kc = 0; kc < chunks; ++kc) {
+            const int s = kc % kStages;
+            if (kc >= kStages && !mbar_wait(&empty[s], ((kc / kStages) - 1) & 1)) {
+                abort_flag = 1;
+                flag_error(p.err, DR_ERRF_TIMEOUT);
+                break;
+            }
+            mbar_expect_tx(&full[s], bytes_a + bytes_b);
+            tma_load_2d(sa + s * bytes_a, &map_w, kc * kChunkK, n0, &full[s]);
+            tma_load_2d(sb + s * bytes_b, &map_h, kc * kChunkK, b0, &full[s]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer
+        const uint32_t idesc = instr_desc(kTileN, p.btile);
+        bool ok = true;
+        for (int kc = 0; kc < chunks; ++kc) {
+            const int s = kc % kStages;
+            if (!mbar_wait(&full[s], (kc / kStages) & 1)) {
+                ok = false;
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+            for (int k = 0; k < kChunkK / 16; ++k) {
+                const uint64_t a = smem_desc(sa + s * bytes_a + k * 32);
+                const uint64_t b = smem_desc(sb + s * bytes_b + k * 32);
+                mma_bf16(tmem, a, b, idesc, (kc | k) != 0);
+            }
+            mma_commit(&empty[s]);   // the stage is free once these MMAs have read it
+        }
+        if (!ok) {
+            abort_flag = 1;
+            flag_error(p.err, DR_ERRF_TIMEOUT);
+        }
+        mma_commit(&done);
+    }
+    __syncwarp();
+
+    // epilogue: warp w owns TMEM lanes (W rows) 32w .. 32w+31
+    const bool finished = __all_sync(0xFFFFFFFFu, mbar_wait(&done, 0));   // warp-uniform for tcgen05.ld
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (!finished) {
+        if (lane == 0) flag_error(p.err, DR_ERRF_TIMEOUT);
+    } else if (!abort_flag) {
+        const int n = n0 + warp * 32 + lane;
+        const int c = n / p.V, v = n - c * p.V;
+        for (int c0 = 0; c0 < p.btile; c0 += 32) {
+            uint32_t r[32];
+            const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0;
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+                "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                  "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+                  "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+                  "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+                  "=r"(r[30]), "=r"(r[31])
+                : "r"(taddr));
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            if (n < N) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int b = b0 + c0 + j;
+                    if (b < p.B) p.logits[((size_t)b * p.C + c) * p.ldv + v] = __uint_as_float(r[j]);
+                }
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols));
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *ptr = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2D bf16 tensor [rows][K] (row stride K*2 bytes), box [box_rows][64], 128-byte swizzle.
+bool encode_2d(CUtensorMap *map, const void *ptr, int rows, int K, int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kChunkK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Batch rows per CTA tile: a multiple of 16 (the MMA's N granularity), at most 256.
+int lm_head_tc_batch_tile(int B) {
+    int t = ((B + 15) / 16) * 16;
+    return t > kMaxBatchTile ? kMaxBatchTile : t;
+}
+
+cudaError_t launch_lm_head_tc(const LmHeadParams &p, int32_t *err, cudaStream_t stream) {
+    const int N = p.C * p.V;
+    TcParams tp;
+    tp.logits = p.logits;
+    tp.B = p.B;
+    tp.K = p.K;
+    tp.C = p.C;
+    tp.V = p.V;
+    tp.ldv = p.ldv;
+    tp.btile = lm_head_tc_batch_tile(p.B);
+    int cols = 32;
+    while (cols < tp.btile) cols <<= 1;
+    tp.tmem_cols = cols;
+    tp.err = err;
+    CUtensorMap map_w, map_h;
+    if (!encode_2d(&map_w, p.W, N, p.K, kTileN) || !encode_2d(&map_h, p.hidden, p.B, p.K, tp.btile))
+        return cudaErrorInvalidValue;
+    const size_t smem = 1024 + (size_t)kStages * (kTileN + tp.btile) * kChunkK * 2;
+    const cudaError_t e = cudaFuncSetAttribute(lm_head_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((p.B + tp.btile - 1) / tp.btile));
+    lm_head_tc_kernel<<<grid, kThreads, smem, stream>>>(map_w, map_h, tp);
+    return cudaGetLastError();
+}
+
+}  // namespace dr

@@ -71,6 +71,7 @@ typedef enum dr_kv_dtype {
 #define DR_ERRF_BLOCK_ID 2 /* a needed block-table entry outside [0, num_blocks); its keys were skipped */
 #define DR_ERRF_POS 4      /* an append position outside [0, capacity) or on an unmapped block; row skipped */
 #define DR_ERRF_TOKEN 8    /* a token outside [0, V) in dr_embed_tokens; that codebook's row was skipped */
+#define DR_ERRF_TIMEOUT 16 /* a bounded on-chip wait gave up (never expected); that CTA's results were not written */
 
 /* Sampler flags. */
 #define DR_SAMPLE_ADVANCE 1 /* after drawing, step[b] += 1 for every row b */
@@ -271,10 +272,15 @@ dr_status dr_embed_tokens(const int32_t *tokens, const void *table, int B, int C
  *   logits : [B][C][ldv] float32 (device), ldv >= V; columns [V, ldv) untouched.
  *            The layout dr_sample_topk_delayed reads.
  *   K      : 256, 512, 768, 1024, 1536 or 2048 (DR_ERR_UNSUPPORTED otherwise)
- * fp32 accumulation; each logit is one dot product in a fixed order.
+ *   err_flag : nullable device int32; DR_ERRF_TIMEOUT if a tensor-core CTA's
+ *            bounded pipeline wait gave up (its logits are then not written)
+ * fp32 accumulation.  Below 16 batch rows each logit is one CUDA-core dot
+ * product in a fixed order; from 16 rows on the head is a dense contraction
+ * on the tensor cores (tcgen05.mma, bf16 in, fp32 accumulate in tensor
+ * memory, K consumed 16 at a time).
  */
 dr_status dr_lm_head(const void *hidden, const void *W, int B, int K, int C, int V, int ldv, float *logits,
-                     void *stream);
+                     int32_t *err_flag, void *stream);
 
 /*
  * dr_plan_splits -- host-only query: how many CTAs (one thread-block
