@@ -210,7 +210,7 @@ class DeviceStep:
         self.emb_out = torch.empty((w.B, 1024), dtype=torch.bfloat16, device=dev)
 
     def run_lm_head(self):
-        self.api.dr_lm_head(self.hidden, self.w_head, self.w.C, self.head_logits)
+        self.api.dr_lm_head(self.hidden, self.w_head, self.w.C, self.head_logits, err_flag=self.err)
 
     def run_embed(self):
         self.api.dr_embed_tokens(self.tokens, self.w_emb, self.w.V, self.emb_out, err_flag=self.err)

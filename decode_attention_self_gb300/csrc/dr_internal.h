@@ -101,7 +101,7 @@ struct LmHeadParams {
 cudaError_t launch_lm_head(const LmHeadParams &p, cudaStream_t stream);
 
 // Batches from this size on run the merged head on the tensor cores (tcgen05).
-constexpr int kLmHeadTensorCoreMinBatch = 16;
+constexpr int kLmHeadTensorCoreMinBatch = 4;
 cudaError_t launch_lm_head_tc(const LmHeadParams &p, int32_t *err, cudaStream_t stream);
 
 }  // namespace dr
