@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     __shared__ float s_wacc[kWarps][kD];
     __shared__ SoftmaxPartial s_part;
 
+    pdl_wait();
     const int h = blockIdx.y;
     // Fused launches carry the B self rows along z, then the cross rows: split
     // like the self rows (z = B + b), or packed one row per CTA (row b =
@@ -326,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
         attend_range<KV, kPaged, kPipelined, false, kSelfRows>(p, false, b, h, key0, key1, -1, qf, warp, lane, m, l,
                                                               acc);
     }
+    pdl_trigger();   // the streaming is done: the next kernel may start launching
     // an e4m3 value is code * v_scale: the kernel accumulates codes and scales the result
     const float out_scale = cross ? 1.0f : p.out_scale;
 
@@ -412,26 +414,15 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
 
 template <typename KV, bool kPaged, bool kPipelined, bool kFused>
 cudaError_t launch_variant(const AttnParams &p, int splits, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
     unsigned zrows = (unsigned)p.B;
     if (kFused && p.xq) zrows += p.xpacked ? (unsigned)((p.B + splits - 1) / splits) : (unsigned)p.B;
-    cfg.gridDim = dim3((unsigned)splits, (unsigned)p.H, zrows);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = splits > 1 ? 1 : 0;
     auto kern = decode_attn_kernel<KV, kPaged, kPipelined, kFused>;
     if (splits > 8) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
-    return cudaLaunchKernelEx(&cfg, kern, p);
+    return launch_kernel(kern, dim3((unsigned)splits, (unsigned)p.H, zrows), dim3(kThreads), 0, stream,
+                         (unsigned)splits, p);
 }
 
 // CTAs of the pipelined kernel that fit on one SM at once (up to 112 registers x 128 threads).

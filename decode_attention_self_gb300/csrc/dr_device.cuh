@@ -67,6 +67,23 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation: it may start while the previous kernel on
+// the stream is finishing, so it waits for that kernel (and the visibility of
+// its writes) before its first global memory access, and lets the next kernel
+// start launching once its own main work is done.  Without the launch
+// attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_wait() {
+#ifndef DR_NO_PDL
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+__device__ __forceinline__ void pdl_trigger() {
+#ifndef DR_NO_PDL
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
 __device__ __forceinline__ void flag_error(int32_t *err, int bits) {
     if (err) atomicOr(err, bits);
 }

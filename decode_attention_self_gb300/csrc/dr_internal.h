@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "dr_api.h"
 
 namespace dr {
@@ -14,6 +16,35 @@ constexpr int kHeadDim = 64;     // D: the only head dimension built
 constexpr int kBlockKeys = 16;   // keys per paged block, and per attention tile
 constexpr int kMaxCodebooks = 16;
 constexpr int kMaxVocab = 2048;
+
+// Launch `kern` with programmatic dependent launch enabled and, when
+// cluster_x > 1, as clusters of cluster_x CTAs along x.
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          unsigned cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+#ifndef DR_NO_PDL
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+#endif
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Largest thread-block cluster used for one (b, h) row of attention.
 int max_cluster_size();

@@ -28,6 +28,8 @@ namespace {
 constexpr int kEmbThreads = 128;
 
 __global__ void __launch_bounds__(kEmbThreads) embed_tokens_kernel(const EmbedParams p) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     const int chunks = p.Dm / 8;
     for (int ch = threadIdx.x; ch < chunks; ch += kEmbThreads) {
@@ -74,6 +76,8 @@ constexpr int kBatch = 16;    // hidden vectors per shared-memory stage
 template <int KC>   // 16-byte chunks per lane per row: K = 256 * KC
 __global__ void __launch_bounds__(kHeadThreads) lm_head_kernel(const LmHeadParams p) {
     extern __shared__ uint4 s_hidden[];   // [kBatch][K/8]
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = (blockIdx.x * kHeadWarps + warp) * kRows;
     const int N = p.C * p.V;
@@ -144,15 +148,13 @@ cudaError_t launch_head(const LmHeadParams &p, cudaStream_t stream) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    kern<<<grid, kHeadThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(kHeadThreads), smem, stream, 1u, p);
 }
 
 }  // namespace
 
 cudaError_t launch_embed_tokens(const EmbedParams &p, cudaStream_t stream) {
-    embed_tokens_kernel<<<(unsigned)p.B, kEmbThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(embed_tokens_kernel, dim3((unsigned)p.B), dim3(kEmbThreads), 0, stream, 1u, p);
 }
 
 cudaError_t launch_lm_head(const LmHeadParams &p, cudaStream_t stream) {

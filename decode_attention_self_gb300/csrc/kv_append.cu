@@ -17,6 +17,8 @@ constexpr int kThreads = 256;
 
 template <bool kPaged, bool kFp8>
 __global__ void __launch_bounds__(kThreads) kv_append_kernel(const AppendParams p) {
+    pdl_wait();
+    pdl_trigger();
     const long long idx = (long long)blockIdx.x * kThreads + threadIdx.x;
     const long long total = (long long)p.B * p.H * 8;
     if (idx >= total) return;
@@ -59,14 +61,9 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const AppendParams 
 cudaError_t launch_kv_append(const AppendParams &p, bool paged, cudaStream_t stream) {
     const long long total = (long long)p.B * p.H * 8;
     const unsigned grid = (unsigned)((total + kThreads - 1) / kThreads);
-    if (p.kv_fp8) {
-        if (paged) kv_append_kernel<true, true><<<grid, kThreads, 0, stream>>>(p);
-        else kv_append_kernel<false, true><<<grid, kThreads, 0, stream>>>(p);
-    } else {
-        if (paged) kv_append_kernel<true, false><<<grid, kThreads, 0, stream>>>(p);
-        else kv_append_kernel<false, false><<<grid, kThreads, 0, stream>>>(p);
-    }
-    return cudaGetLastError();
+    auto kern = p.kv_fp8 ? (paged ? kv_append_kernel<true, true> : kv_append_kernel<false, true>)
+                         : (paged ? kv_append_kernel<true, false> : kv_append_kernel<false, false>);
+    return launch_kernel(kern, dim3(grid), dim3(kThreads), 0, stream, 1u, p);
 }
 
 }  // namespace dr

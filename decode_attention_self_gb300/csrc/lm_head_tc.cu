@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileN;
     const int b0 = blockIdx.y * p.btile;
@@ -183,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
 
+    pdl_trigger();
     // epilogue: warp w owns TMEM lanes (W rows) 32w .. 32w+31
     const bool finished = __all_sync(0xFFFFFFFFu, mbar_wait(&done, 0));   // warp-uniform for tcgen05.ld
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -276,8 +278,7 @@ cudaError_t launch_lm_head_tc(const LmHeadParams &p, int32_t *err, cudaStream_t 
                                                (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((p.B + tp.btile - 1) / tp.btile));
-    lm_head_tc_kernel<<<grid, kThreads, smem, stream>>>(map_w, map_h, tp);
-    return cudaGetLastError();
+    return launch_kernel(lm_head_tc_kernel, grid, dim3(kThreads), smem, stream, 1u, map_w, map_h, tp);
 }
 
 }  // namespace dr

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) 
     __shared__ float s_rf[kWarps];
     __shared__ int s_ri[kWarps];
 
+    pdl_wait();
     const int c = blockIdx.x;
     const int b = blockIdx.y;
     const int t = threadIdx.x;
@@ -299,6 +300,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) 
         }
     }
 
+    pdl_trigger();
     if (p.flags & DR_SAMPLE_ADVANCE) {
         // every thread of every codebook CTA of this row has read step[b] before it changes
         if (gridDim.x > 1) cg::this_cluster().sync();
@@ -309,23 +311,14 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) 
 
 template <int EPT>
 cudaError_t launch_ept(const SampleParams &p, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.C, (unsigned)p.B, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = ((p.flags & DR_SAMPLE_ADVANCE) && p.C > 1) ? 1 : 0;
+    const bool clustered = (p.flags & DR_SAMPLE_ADVANCE) && p.C > 1;
     auto kern = sample_kernel<EPT>;
-    if (cfg.numAttrs && p.C > 8) {
+    if (clustered && p.C > 8) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
-    return cudaLaunchKernelEx(&cfg, kern, p);
+    return launch_kernel(kern, dim3((unsigned)p.C, (unsigned)p.B, 1), dim3(kThreads), 0, stream,
+                         clustered ? (unsigned)p.C : 1u, p);
 }
 
 }  // namespace
