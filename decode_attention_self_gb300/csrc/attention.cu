@@ -48,28 +48,35 @@ struct SoftmaxPartial {
     float acc[kD];   // sum of 2^(s - m) * v
 };
 
-// Storage formats of a KV cache.  One lane moves the 8 consecutive dims of one
-// key that it owns: 16 bytes of bf16 or 8 bytes of e4m3 codes.
+// Storage formats of a KV cache and the lane layout that streams them.  A key's
+// 64 dims are spread over kLanesPerKey lanes, each moving kDims consecutive
+// dims: 8 bf16 (16 bytes) or 8 e4m3 codes (8 bytes), so one load instruction
+// of a warp reads 4 consecutive key rows (512 or 256 contiguous bytes).
+// (Four lanes per key with 16 e4m3 codes each was measured slower: the extra
+// merge level and register pressure outweighed the shorter reductions.)
 struct Bf16Kv {
     using Chunk = uint4;
     static constexpr int kElemBytes = 2;
+    static constexpr int kLanesPerKey = 8;
+    static constexpr int kDims = 8;   // dims per lane: [sub*8, sub*8 + 8)
     __device__ static Chunk zero() { return make_uint4(0, 0, 0, 0); }
     __device__ static Chunk load(const uint8_t *p) { return ld_stream16(p); }
     __device__ static void store(uint8_t *p, const Chunk &c) { *reinterpret_cast<uint4 *>(p) = c; }
-    __device__ static void unpack(const Chunk &c, float (&f)[8]) { unpack8(c, f); }
-    // This step's key/value (bf16) in the cache's format.
-    __device__ static Chunk from_bf16(const uint4 &w, float) { return w; }
+    __device__ static void unpack(const Chunk &c, float (&f)[kDims]) { unpack8(c, f); }
+    // This step's key/value (bf16 dims of this lane) in the cache's format.
+    __device__ static Chunk from_bf16(const uint16_t *src, float) { return ld_ro16(src); }
 };
-
 struct Fp8Kv {
     using Chunk = uint2;
     static constexpr int kElemBytes = 1;
+    static constexpr int kLanesPerKey = 8;
+    static constexpr int kDims = 8;
     __device__ static Chunk zero() { return make_uint2(0, 0); }
     __device__ static Chunk load(const uint8_t *p) { return ld_stream8(p); }
     __device__ static void store(uint8_t *p, const Chunk &c) { *reinterpret_cast<uint2 *>(p) = c; }
-    __device__ static void unpack(const Chunk &c, float (&f)[8]) { unpack8_e4m3(c, f); }
+    __device__ static void unpack(const Chunk &c, float (&f)[kDims]) { unpack8_e4m3(c, f); }
     // Quantise: code = e4m3(fl32(x / scale)), round to nearest even, saturating.
-    __device__ static Chunk from_bf16(const uint4 &w, float scale) { return quantize8_e4m3(w, scale); }
+    __device__ static Chunk from_bf16(const uint16_t *src, float scale) { return quantize8_e4m3(ld_ro16(src), scale); }
 };
 
 // Merge (m2, l2, a2) into (m, l, a); an empty state has m = -inf, l = 0, a = 0.
@@ -92,43 +99,47 @@ __device__ __forceinline__ void merge_state(float &m, float &l, float (&a)[N], f
 // gives the same softmax: states carry (m, l, acc) relative to their own m.
 constexpr float kRescaleSlack = 8.0f;
 
-// One lane group's online-softmax update with a 16-key tile: this lane holds
-// dims 8*sub..8*sub+7 of keys t+grp, t+grp+4, t+grp+8, t+grp+12.  kFull: every
-// key of the tile is valid (no masking).
+// One lane group's online-softmax update with a 16-key tile.  With G = 32 /
+// kLanesPerKey lane groups, group grp holds keys t + grp + G*u (u < 16 / G) and
+// this lane the kDims dims [sub*kDims, (sub+1)*kDims) of each.  kFull: every key
+// of the tile is valid (no masking).
 template <typename KV, bool kFull>
-__device__ __forceinline__ void consume_tile(const typename KV::Chunk (&kw)[4], const typename KV::Chunk (&vw)[4],
-                                             const float (&qf)[8], int t, int grp, int key1, float &m, float &l,
-                                             float (&acc)[8]) {
-    float sc[4];
+__device__ __forceinline__ void consume_tile(const typename KV::Chunk (&kw)[16 * KV::kLanesPerKey / 32],
+                                             const typename KV::Chunk (&vw)[16 * KV::kLanesPerKey / 32],
+                                             const float (&qf)[KV::kDims], int t, int grp, int key1, float &m,
+                                             float &l, float (&acc)[KV::kDims]) {
+    constexpr int kLpk = KV::kLanesPerKey, kGroups = 32 / kLpk, kKeys = kTile / kGroups, kDims = KV::kDims;
+    float sc[kKeys];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        float kf[8];
+    for (int u = 0; u < kKeys; ++u) {
+        float kf[kDims];
         KV::unpack(kw[u], kf);
         float d = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) d = fmaf(qf[j], kf[j], d);
-        d += __shfl_xor_sync(0xFFFFFFFFu, d, 1);
-        d += __shfl_xor_sync(0xFFFFFFFFu, d, 2);
-        d += __shfl_xor_sync(0xFFFFFFFFu, d, 4);
-        sc[u] = (kFull || t + grp + 4 * u < key1) ? d : -INFINITY;
+        for (int j = 0; j < kDims; ++j) d = fmaf(qf[j], kf[j], d);
+#pragma unroll
+        for (int off = 1; off < kLpk; off <<= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, off);
+        sc[u] = (kFull || t + grp + kGroups * u < key1) ? d : -INFINITY;
     }
-    const float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+    float mt = sc[0];
+#pragma unroll
+    for (int u = 1; u < kKeys; ++u) mt = fmaxf(mt, sc[u]);
     if (mt > m + kRescaleSlack) {   // also taken for the first valid key (m = -inf)
         const float corr = fast_exp2(m - mt);
         l *= corr;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] *= corr;
+        for (int j = 0; j < kDims; ++j) acc[j] *= corr;
         m = mt;
     }
     if (m == -INFINITY) return;   // this lane group had no valid key yet
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kKeys; ++u) {
         const float pu = fast_exp2(sc[u] - m);
         l += pu;
-        float vf[8];
+        float vf[kDims];
         KV::unpack(vw[u], vf);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(pu, vf[j], acc[j]);
+        for (int j = 0; j < kDims; ++j) acc[j] = fmaf(pu, vf[j], acc[j]);
     }
 }
 
@@ -144,38 +155,60 @@ enum RowKind { kSelfRows, kCrossRows, kEitherRows };
 // parameters are read from the parameter space, not copied into registers.
 template <typename KV, bool kPaged, bool kPipelined, bool kAppend, RowKind kKind>
 __device__ __forceinline__ void attend_range(const AttnParams &p, bool cross_row, int b, int h, int key0, int key1,
-                                             int newpos, const float (&qf)[8], int warp, int lane, float &m, float &l,
-                                             float (&acc)[8]) {
+                                             int newpos, int warp, int lane, float *s_wm, float *s_wl,
+                                             float (*s_wacc)[kD]) {
     using Chunk = typename KV::Chunk;
+    constexpr int kLpk = KV::kLanesPerKey, kGroups = 32 / kLpk, kKeys = kTile / kGroups, kDims = KV::kDims;
     constexpr size_t kRowBytes = (size_t)kD * KV::kElemBytes;
-    const int grp = lane >> 3, sub = lane & 7;
+    const int grp = lane / kLpk, sub = lane % kLpk;
     const size_t row = (size_t)b * p.H + h;
     const bool cross = kKind == kCrossRows || (kKind == kEitherRows && cross_row);
     const bool paged = kPaged && !cross;
     const uint8_t *kc = reinterpret_cast<const uint8_t *>(cross ? p.xk : p.k);
     const uint8_t *vc = reinterpret_cast<const uint8_t *>(cross ? p.xv : p.v);
+    const size_t lane_off = (size_t)sub * kDims * KV::kElemBytes;   // this lane's chunk of a key row
+
+    // this lane's query dims, pre-scaled (the softmax scale in log2 units; times k_scale for e4m3)
+    float qf[kDims];
+    {
+        const uint16_t *qrow = (cross ? p.xq : p.q) + row * kD + sub * kDims;
+        const float qscale = cross ? p.xqscale : p.qscale;
+#pragma unroll
+        for (int c8 = 0; c8 < kDims / 8; ++c8) {
+            float f[8];
+            unpack8(ld_ro16(qrow + 8 * c8), f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) qf[8 * c8 + j] = f[j] * qscale;
+        }
+    }
+    float m = -INFINITY, l = 0.f;
+    float acc[kDims];
+#pragma unroll
+    for (int j = 0; j < kDims; ++j) acc[j] = 0.f;
 
     // Issue the loads of tile t (zeros past key1 or for an unmapped block).  With
     // kAppend, the key at newpos is this step's k_new/v_new, converted to the
     // cache format, stored into its cache slot and used from registers.
-    auto load_tile = [&](int t, Chunk (&kw)[4], Chunk (&vw)[4]) -> bool {
-        size_t base = 0;
-        bool ok = true;
+    auto tile_base = [&](int t, bool &ok) -> size_t {
+        ok = true;
         if (paged) {
             const int blk = __ldg(p.table + (size_t)b * p.max_blocks + t / kTile);
             ok = (unsigned)blk < (unsigned)p.num_blocks;
-            base = ok ? ((size_t)blk * p.H + h) * (size_t)kTile * kRowBytes : 0;
-        } else {
-            base = (row * (size_t)(cross ? p.xcap : p.cap) + (size_t)t) * kRowBytes;
+            return ok ? ((size_t)blk * p.H + h) * (size_t)kTile * kRowBytes : 0;
         }
+        return (row * (size_t)(cross ? p.xcap : p.cap) + (size_t)t) * kRowBytes;
+    };
+    auto load_tile = [&](int t, Chunk (&kw)[kKeys], Chunk (&vw)[kKeys]) -> bool {
+        bool ok;
+        const size_t base = tile_base(t, ok);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int rr = grp + 4 * u;
-            const size_t off = base + (size_t)rr * kRowBytes + (size_t)sub * 8 * KV::kElemBytes;
+        for (int u = 0; u < kKeys; ++u) {
+            const int rr = grp + kGroups * u;
+            const size_t off = base + (size_t)rr * kRowBytes + lane_off;
             if (ok && t + rr < key1) {
                 if (kAppend && t + rr == newpos) {
-                    kw[u] = KV::from_bf16(ld_ro16(p.k_new + row * kD + sub * 8), p.k_scale);
-                    vw[u] = KV::from_bf16(ld_ro16(p.v_new + row * kD + sub * 8), p.v_scale);
+                    kw[u] = KV::from_bf16(p.k_new + row * kD + sub * kDims, p.k_scale);
+                    vw[u] = KV::from_bf16(p.v_new + row * kD + sub * kDims, p.v_scale);
                     KV::store(const_cast<uint8_t *>(kc) + off, kw[u]);
                     KV::store(const_cast<uint8_t *>(vc) + off, vw[u]);
                 } else {
@@ -190,40 +223,32 @@ __device__ __forceinline__ void attend_range(const AttnParams &p, bool cross_row
         if (kAppend && !ok && t <= newpos && newpos < t + kTile && lane == 0) flag_error(p.err, DR_ERRF_POS);
         return ok;
     };
-
     // Whole tiles away from the appended key need no per-key checks.
     auto full_tile = [&](int t) -> bool {
         return t + kTile <= key1 && !(kAppend && newpos >= t && newpos < t + kTile);
     };
-    auto load_full = [&](int t, Chunk (&kw)[4], Chunk (&vw)[4]) -> bool {
-        size_t base = 0;
-        bool ok = true;
-        if (paged) {
-            const int blk = __ldg(p.table + (size_t)b * p.max_blocks + t / kTile);
-            ok = (unsigned)blk < (unsigned)p.num_blocks;
-            base = ok ? ((size_t)blk * p.H + h) * (size_t)kTile * kRowBytes : 0;
-        } else {
-            base = (row * (size_t)(cross ? p.xcap : p.cap) + (size_t)t) * kRowBytes;
-        }
+    auto load_full = [&](int t, Chunk (&kw)[kKeys], Chunk (&vw)[kKeys]) -> bool {
+        bool ok;
+        const size_t base = tile_base(t, ok);
         if (ok) {
-            const uint8_t *kp = kc + base + (size_t)grp * kRowBytes + (size_t)sub * 8 * KV::kElemBytes;
-            const uint8_t *vp = vc + base + (size_t)grp * kRowBytes + (size_t)sub * 8 * KV::kElemBytes;
+            const uint8_t *kp = kc + base + (size_t)grp * kRowBytes + lane_off;
+            const uint8_t *vp = vc + base + (size_t)grp * kRowBytes + lane_off;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                kw[u] = KV::load(kp + 4 * u * kRowBytes);
-                vw[u] = KV::load(vp + 4 * u * kRowBytes);
+            for (int u = 0; u < kKeys; ++u) {
+                kw[u] = KV::load(kp + (size_t)kGroups * u * kRowBytes);
+                vw[u] = KV::load(vp + (size_t)kGroups * u * kRowBytes);
             }
         }
         return ok;
     };
 
     if constexpr (kPipelined) {
-        Chunk kw[4], vw[4];
+        Chunk kw[kKeys], vw[kKeys];
         int t = key0 + warp * kTile;
         bool full = t < key1 && full_tile(t);
         bool ok = t < key1 ? (full ? load_full(t, kw, vw) : load_tile(t, kw, vw)) : true;
         for (; t < key1; t += kWarps * kTile) {
-            Chunk nk[4] = {}, nv[4] = {};
+            Chunk nk[kKeys] = {}, nv[kKeys] = {};
             const int tn = t + kWarps * kTile;
             const bool nfull = tn < key1 && full_tile(tn);
             const bool nok = tn < key1 ? (nfull ? load_full(tn, nk, nv) : load_tile(tn, nk, nv)) : true;
@@ -235,7 +260,7 @@ __device__ __forceinline__ void attend_range(const AttnParams &p, bool cross_row
                 consume_tile<KV, false>(kw, vw, qf, t, grp, key1, m, l, acc);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kKeys; ++u) {
                 kw[u] = nk[u];
                 vw[u] = nv[u];
             }
@@ -244,7 +269,7 @@ __device__ __forceinline__ void attend_range(const AttnParams &p, bool cross_row
         }
     } else {
         for (int t = key0 + warp * kTile; t < key1; t += kWarps * kTile) {
-            Chunk kw[4], vw[4];
+            Chunk kw[kKeys], vw[kKeys];
             if (full_tile(t)) {
                 if (load_full(t, kw, vw)) consume_tile<KV, true>(kw, vw, qf, t, grp, key1, m, l, acc);
                 else if (lane == 0) flag_error(p.err, DR_ERRF_BLOCK_ID);
@@ -253,6 +278,26 @@ __device__ __forceinline__ void attend_range(const AttnParams &p, bool cross_row
                 else if (lane == 0) flag_error(p.err, DR_ERRF_BLOCK_ID);
             }
         }
+    }
+
+    // Lanes sub, sub + kLpk, ... hold the same dims for different keys: merge them,
+    // then lane group 0 publishes the warp's partial state.
+#pragma unroll
+    for (int off = kLpk; off < 32; off <<= 1) {
+        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
+        const float l2 = __shfl_xor_sync(0xFFFFFFFFu, l, off);
+        float a2[kDims];
+#pragma unroll
+        for (int j = 0; j < kDims; ++j) a2[j] = __shfl_xor_sync(0xFFFFFFFFu, acc[j], off);
+        merge_state(m, l, acc, m2, l2, a2);
+    }
+    if (grp == 0) {
+        if (sub == 0) {
+            s_wm[warp] = m;
+            s_wl[warp] = l;
+        }
+#pragma unroll
+        for (int j = 0; j < kDims; ++j) s_wacc[warp][sub * kDims + j] = acc[j];
     }
 }
 
@@ -281,8 +326,6 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     if (b >= p.B) return;   // tail of the packed region (no cluster barrier is reached there)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int grp = lane >> 3;
-    const int sub = lane & 7;
 
     const size_t row = (size_t)b * p.H + h;
     const int cap = cross ? p.xcap : p.cap;
@@ -302,53 +345,24 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     const int key0 = min(split * per, ntiles) * kTile;
     const int key1 = min(key0 + per * kTile, L);
 
-    float qf[8];
-    unpack8(ld_ro16((cross ? p.xq : p.q) + row * kD + sub * 8), qf);
-    const float qscale = cross ? p.xqscale : p.qscale;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) qf[j] *= qscale;
-
-    float m = -INFINITY, l = 0.f;
-    float acc[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-
     if constexpr (kFused && std::is_same<KV, Bf16Kv>::value) {
-        attend_range<KV, kPaged, kPipelined, true, kEitherRows>(p, cross, b, h, key0, key1, newpos, qf, warp, lane, m,
-                                                                 l, acc);
+        attend_range<KV, kPaged, kPipelined, true, kEitherRows>(p, cross, b, h, key0, key1, newpos, warp, lane, s_wm,
+                                                                 s_wl, s_wacc);
     } else if constexpr (kFused) {
         if (cross)
-            attend_range<Bf16Kv, false, kPipelined, false, kCrossRows>(p, true, b, h, key0, key1, -1, qf, warp, lane, m,
-                                                                      l, acc);
+            attend_range<Bf16Kv, false, kPipelined, false, kCrossRows>(p, true, b, h, key0, key1, -1, warp, lane, s_wm,
+                                                                      s_wl, s_wacc);
         else
-            attend_range<KV, kPaged, kPipelined, true, kSelfRows>(p, false, b, h, key0, key1, newpos, qf, warp, lane, m,
-                                                                 l, acc);
+            attend_range<KV, kPaged, kPipelined, true, kSelfRows>(p, false, b, h, key0, key1, newpos, warp, lane, s_wm,
+                                                                 s_wl, s_wacc);
     } else {
-        attend_range<KV, kPaged, kPipelined, false, kSelfRows>(p, false, b, h, key0, key1, -1, qf, warp, lane, m, l,
-                                                              acc);
+        attend_range<KV, kPaged, kPipelined, false, kSelfRows>(p, false, b, h, key0, key1, -1, warp, lane, s_wm, s_wl,
+                                                              s_wacc);
     }
     pdl_trigger();   // the streaming is done: the next kernel may start launching
     // an e4m3 value is code * v_scale: the kernel accumulates codes and scales the result
     const float out_scale = cross ? 1.0f : p.out_scale;
 
-    // Lanes sub, sub+8, sub+16, sub+24 hold the same dims for different keys.
-#pragma unroll
-    for (int off = 8; off <= 16; off <<= 1) {
-        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
-        const float l2 = __shfl_xor_sync(0xFFFFFFFFu, l, off);
-        float a2[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) a2[j] = __shfl_xor_sync(0xFFFFFFFFu, acc[j], off);
-        merge_state(m, l, acc, m2, l2, a2);
-    }
-    if (grp == 0) {
-        if (sub == 0) {
-            s_wm[warp] = m;
-            s_wl[warp] = l;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s_wacc[warp][sub * 8 + j] = acc[j];
-    }
     __syncthreads();
     if (threadIdx.x < kD) {
         const int d = threadIdx.x;
