@@ -155,18 +155,24 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
+def sources_digest(names) -> str:
+    """First 16 hex digits of the SHA-256 of the named csrc files, concatenated in order."""
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "decode_attention_self_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def committed_traffic(kernel_key: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged since."""
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's sources (its code and the launch
+    planning) are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(kernel_key)
-    if not rec:
-        return None
-    src = os.path.join(ROOT, "decode_attention_self_gb300", "csrc", rec["source"])
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if digest != rec.get("source_sha256_16"):
+    if not rec or sources_digest(rec["sources"]) != rec.get("sources_sha256_16"):
         return None
     return rec
 
@@ -480,7 +486,7 @@ def main():
     dom_bytes = sb["self"] + sb["cross"] + sb["append"] if ds.fused else sb["self"]
     achieved = dom_bytes / (self_avg_ms * 1e-3) / 1e9
     kname = "decode_attn_kernel<fused>" if ds.fused else "decode_attn_kernel"
-    traffic = committed_traffic(f"{kname} workload {w.index}")
+    traffic = committed_traffic(f"{kname} workload {w.index} {'e4m3' if args.kv == 'fp8' else 'bf16'}")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
                 "kernel": kname + (" (dr_decode_layer: append + self + cross)" if ds.fused else " (dr_decode_self_attn)"),

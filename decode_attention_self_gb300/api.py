@@ -48,7 +48,7 @@ _lib.dr_decode_layer.argtypes = [_vp, ctypes.POINTER(dr_kv_cache), _vp, _vp, _vp
 _lib.dr_sample_topk_delayed.argtypes = [_vp, _i, _i, _i, _i, _f, _i, _vp, _vp, ctypes.c_int32, _vp, _vp, _i, _vp]
 _lib.dr_embed_tokens.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _i, _vp, _vp]
 _lib.dr_lm_head.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp]
-_lib.dr_plan_splits.argtypes = [_i, _i, _i, _i]
+_lib.dr_plan_splits.argtypes = [_i, _i, _i, _i, _i]
 _lib.dr_plan_splits.restype = _i
 _lib.dr_status_string.argtypes = [_i]
 _lib.dr_status_string.restype = ctypes.c_char_p
@@ -67,8 +67,8 @@ def dr_status_string(status: int) -> str:
     return _lib.dr_status_string(int(status)).decode()
 
 
-def dr_plan_splits(B: int, H: int, max_len: int, num_sms: int) -> int:
-    return int(_lib.dr_plan_splits(B, H, max_len, num_sms))
+def dr_plan_splits(B: int, H: int, max_len: int, kv_dtype: int, num_sms: int) -> int:
+    return int(_lib.dr_plan_splits(B, H, max_len, kv_dtype, num_sms))
 
 
 def _check(fn: str, status: int):

@@ -114,9 +114,12 @@ __device__ __forceinline__ void consume_tile(const typename KV::Chunk (&kw)[16 *
     for (int u = 0; u < kKeys; ++u) {
         float kf[kDims];
         KV::unpack(kw[u], kf);
-        float d = 0.f;
+        // even and odd dims in two partial sums: one packed f32x2 FMA per pair of dims
+        float2 d2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < kDims; ++j) d = fmaf(qf[j], kf[j], d);
+        for (int j = 0; j < kDims; j += 2)
+            d2 = __ffma2_rn(make_float2(qf[j], qf[j + 1]), make_float2(kf[j], kf[j + 1]), d2);
+        float d = d2.x + d2.y;
 #pragma unroll
         for (int off = 1; off < kLpk; off <<= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, off);
         sc[u] = (kFull || t + grp + kGroups * u < key1) ? d : -INFINITY;
@@ -139,7 +142,12 @@ __device__ __forceinline__ void consume_tile(const typename KV::Chunk (&kw)[16 *
         float vf[kDims];
         KV::unpack(vw[u], vf);
 #pragma unroll
-        for (int j = 0; j < kDims; ++j) acc[j] = fmaf(pu, vf[j], acc[j]);
+        for (int j = 0; j < kDims; j += 2) {   // packed f32x2 FMA: two IEEE fmas per instruction
+            const float2 a = __ffma2_rn(make_float2(pu, pu), make_float2(vf[j], vf[j + 1]),
+                                        make_float2(acc[j], acc[j + 1]));
+            acc[j] = a.x;
+            acc[j + 1] = a.y;
+        }
     }
 }
 

@@ -113,32 +113,41 @@ dr_status check_attn_args(const void *q, const int32_t *lens, void *out, dr_dtyp
     return DR_OK;
 }
 
+int length_bound(const dr::AttnParams &p, int hint) { return (hint > 0 && hint < p.cap) ? hint : p.cap; }
+
+int self_splits(const dr::AttnParams &p, int hint, int sms) {
+    return dr_plan_splits(p.B, p.H, length_bound(p, hint), p.kv_fp8 ? DR_KV_FP8_E4M3 : DR_KV_BF16, sms);
+}
+
 dr_status launch(const dr::AttnParams &p, bool paged, int hint, void *stream) {
-    const int bound = (hint > 0 && hint < p.cap) ? hint : p.cap;
     const int sms = dr::current_device_sms();
     if (sms <= 0) return DR_ERR_CUDA;
-    const int splits = dr_plan_splits(p.B, p.H, bound, sms);
-    return from_cuda(dr::launch_decode_attn(p, paged, splits, static_cast<cudaStream_t>(stream)));
+    return from_cuda(dr::launch_decode_attn(p, paged, self_splits(p, hint, sms), static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
 
 extern "C" {
 
-int dr_plan_splits(int B, int H, int max_len, int num_sms) {
+int dr_plan_splits(int B, int H, int max_len, int kv_dtype, int num_sms) {
     if (B < 1 || H < 1 || max_len < 1 || num_sms < 1) return 1;
+    if (kv_dtype != DR_KV_BF16 && kv_dtype != DR_KV_FP8_E4M3) return 1;
+    constexpr long long kCtaBytes = 256 * 1024;   // K+V bytes per CTA at the longest row
+    constexpr long long kFillCtasPerSm = 6;
     const long long rows = (long long)B * H;
-    const int tiles = (max_len + dr::kBlockKeys - 1) / dr::kBlockKeys;
-    // At most 512 keys (32 tiles, 128 KiB of K+V) per CTA at the longest row...
-    int s = (tiles + 31) / 32;
-    // ...and at least two CTAs per SM when the batch alone cannot fill the GPU...
-    const long long fill = (2LL * num_sms + rows - 1) / rows;
-    if (fill > s) s = (int)(fill < 64 ? fill : 64);
+    const long long key_bytes = 2LL * dr::kHeadDim * (kv_dtype == DR_KV_FP8_E4M3 ? 1 : 2);
+    const long long tiles = (max_len + dr::kBlockKeys - 1) / dr::kBlockKeys;
+    // At most kCtaBytes of K+V per CTA at the longest row: ragged rows spread
+    // evenly, and each CTA streams enough to amortise its share of the merge...
+    long long s = ((long long)max_len * key_bytes + kCtaBytes - 1) / kCtaBytes;
+    // ...and at least kFillCtasPerSm CTAs per SM when the rows alone are fewer...
+    const long long fill = (kFillCtasPerSm * num_sms + rows - 1) / rows;
+    if (fill > s) s = fill;
     // ...but never fewer than 4 tiles (64 keys) per CTA, nor more than one cluster.
-    const int by_tiles = (tiles + 3) / 4;
+    const long long by_tiles = (tiles + 3) / 4;
     if (s > by_tiles) s = by_tiles;
     if (s > dr::max_cluster_size()) s = dr::max_cluster_size();
-    return s < 1 ? 1 : s;
+    return s < 1 ? 1 : (int)s;
 }
 
 dr_status dr_kv_append(const dr_kv_cache *cache, const void *k_new, const void *v_new, const int32_t *pos, int B,
@@ -222,12 +231,17 @@ dr_status dr_decode_layer(const void *q, const dr_kv_cache *cache, const void *k
     p.xlens = enc_len;
     p.xcap = Lc_max;
     p.xout = out_cross;
-    // Cross rows that the standalone plan gives one CTA each are packed one per CTA;
-    // longer ones are split like the self rows.
+    // A description row takes one CTA of its own (packed, one row per CTA) when
+    // the standalone plan gives it one, or when it is no longer than one self
+    // CTA's share of the longest self row; otherwise it is split like the self rows.
     const int sms = dr::current_device_sms();
     if (sms <= 0) return DR_ERR_CUDA;
-    p.xpacked = dr_plan_splits(B, H, Lc_max, sms) == 1;
-    return launch(p, paged, max_seq_len_hint, stream);
+    const int s_self = self_splits(p, max_seq_len_hint, sms);
+    const int self_tiles = (length_bound(p, max_seq_len_hint) + dr::kBlockKeys - 1) / dr::kBlockKeys;
+    const int cross_tiles = (Lc_max + dr::kBlockKeys - 1) / dr::kBlockKeys;
+    p.xpacked = dr_plan_splits(B, H, Lc_max, DR_KV_BF16, sms) == 1 ||
+                cross_tiles <= (self_tiles + s_self - 1) / s_self;
+    return from_cuda(dr::launch_decode_attn(p, paged, s_self, static_cast<cudaStream_t>(stream)));
 }
 
 dr_status dr_sample_topk_delayed(const float *logits, int B, int C, int V, int ldv, float temperature, int top_k,

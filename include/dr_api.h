@@ -285,11 +285,16 @@ dr_status dr_lm_head(const void *hidden, const void *W, int B, int K, int C, int
 /*
  * dr_plan_splits -- host-only query: how many CTAs (one thread-block
  * cluster) share each (b, h) row of an attention call with this batch,
- * head count and length bound on a GPU with num_sms SMs.  Each CTA of the
- * cluster takes an equal run of whole 16-key blocks of the row.  Pure
- * arithmetic; touches no device.
+ * head count, length bound and KV storage type (DR_KV_BF16 or
+ * DR_KV_FP8_E4M3; the description-encoder rows of dr_decode_cross_attn are
+ * DR_KV_BF16) on a GPU with num_sms SMs.  Each CTA of the cluster takes an
+ * equal run of whole 16-key blocks of the row.  The plan: at most 256 KiB
+ * of K+V per CTA at the longest row, at least 6 CTAs per SM when the rows
+ * alone are fewer, at least 64 keys per CTA, at most 8 CTAs.  Pure
+ * arithmetic; touches no device.  Returns 1 for non-positive sizes or an
+ * unknown kv_dtype.
  */
-int dr_plan_splits(int B, int H, int max_len, int num_sms);
+int dr_plan_splits(int B, int H, int max_len, int kv_dtype, int num_sms);
 
 /* Static, NUL-terminated description of a status code. */
 const char *dr_status_string(dr_status s);

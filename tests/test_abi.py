@@ -117,11 +117,16 @@ def test_sampler_validation(lib):
 
 
 def test_split_plan(lib):
-    # split count per (b, h) row: one cluster of at most 8 CTAs, >= 64 keys each, <= 512 keys each at
-    # the longest row when possible, and enough CTAs to cover a 152-SM GPU twice at small batch.
+    # split count per (b, h) row: one cluster of at most 8 CTAs, >= 64 keys each, <= 256 KiB of K+V each at
+    # the longest row, and at least 6 CTAs per SM of a 152-SM GPU when the rows alone are fewer.
     plan = lib.dr_plan_splits
-    assert plan(128, 16, 4096, 152) == 8      # batch 128, rows up to 4096 keys: 512 keys per CTA
-    assert plan(32, 16, 2048, 152) == 4       # batch 32, rows up to 2048 keys
-    assert plan(1, 16, 1024, 152) == 8        # batch 1: fill the GPU, capped by the cluster size
-    assert plan(1, 16, 64, 152) == 1          # a 64-key row is one CTA
-    assert plan(1, 16, 200, 152) == 4         # 13 tiles, at least 4 per CTA: ceil(13 / 4) = 4 CTAs
+    BF16, E4M3 = 0, 1
+    assert plan(128, 16, 4096, BF16, 152) == 4    # 4096 keys x 256 B = 1 MiB per row: 4 CTAs
+    assert plan(128, 16, 4096, E4M3, 152) == 2    # 128 B per key: 2 CTAs
+    assert plan(32, 16, 2048, BF16, 152) == 2     # 512 rows: 2 CTAs each cover 6 x 152 = 912
+    assert plan(16, 16, 1024, BF16, 152) == 4     # 256 rows: ceil(912 / 256) = 4
+    assert plan(1, 16, 1024, BF16, 152) == 8      # batch 1: fill the GPU, capped by the cluster size
+    assert plan(1, 16, 64, BF16, 152) == 1        # a 64-key row is one CTA
+    assert plan(1, 16, 200, BF16, 152) == 4       # 13 tiles, at least 4 per CTA: ceil(13 / 4) = 4 CTAs
+    assert plan(128, 16, 4096, 7, 152) == 1       # unknown storage type
+    assert plan(0, 16, 4096, BF16, 152) == 1

@@ -114,6 +114,26 @@ def test_ragged_lengths_and_split_counts(api, cuda_device, layout, hint):
     assert_attn_close(out, oracle_self(w, cache, q, default_scale(D)), f"{layout} hint {hint}")
 
 
+# Batch sizes whose 16-head rows give each split count for a 1024-key bound on 152 SMs: the plan asks for
+# ceil(6 * 152 / (16 B)) CTAs per row (at most 8), and 256 KiB per CTA needs only one.
+SPLIT_BATCHES = {8: 8, 9: 7, 10: 6, 12: 5, 15: 4, 20: 3, 29: 2, 57: 1}
+
+
+@pytest.mark.parametrize("B", sorted(SPLIT_BATCHES))
+def test_every_split_count(api, cuda_device, B):
+    S = SPLIT_BATCHES[B]
+    assert api.dr_plan_splits(B, 16, 1024, api.DR_KV_BF16, 152) == S
+    rng = np.random.default_rng(B)
+    # ragged rows, with short rows that leave some CTAs of their cluster without a tile
+    lens = [1024, 1, 16, 17] + [int(x) for x in rng.integers(1, 1024, size=B - 4, endpoint=True)]
+    w, cache, q = ragged_case("paged", lens, 1024, seed=20 + B)
+    kv = to_dev(cache, cuda_device)
+    out = torch.empty((w.B, w.H, D), dtype=torch.float32, device=cuda_device)
+    api.dr_decode_self_attn(q.to(cuda_device), kv, torch.from_numpy(w.seq_len).to(cuda_device), out,
+                            max_seq_len_hint=1024)
+    assert_attn_close(out, oracle_self(w, cache, q, default_scale(D)), f"B={B}, {S} CTAs per row")
+
+
 @pytest.mark.parametrize("L", [1, 17, 1000, 4095, 4096])
 def test_batch1_long_rows(api, cuda_device, L):
     w, cache, q = ragged_case("contiguous", [L], 4096, seed=3)
@@ -272,13 +292,15 @@ def test_calls_capture_into_a_cuda_graph(api, cuda_device):
 
 def test_row_result_independent_of_batch_and_kernel_variant(api, cuda_device):
     # A row alone (B=1: the whole grid is resident, the pipelined variant runs) and the same row inside a
-    # batch of 96 (the streaming variant runs) share the split plan (8 CTAs per row for a 4096-key bound),
-    # and the two variants do the same arithmetic in the same order: the outputs must be bit-identical.
+    # batch of 8 (1024 CTAs, more than 4 per SM: the streaming variant runs) share the split plan (8 CTAs
+    # per row for a 4096-key bound), and the two variants do the same arithmetic in the same order: the
+    # outputs must be bit-identical.
     from decode_attention_self_gb300 import api as _api
     dev = cuda_device
-    lens = [4000] + [int(x) for x in np.random.default_rng(13).integers(1000, 4096, size=95)]
+    lens = [4000] + [int(x) for x in np.random.default_rng(13).integers(1000, 4096, size=7)]
     w, cache, q = ragged_case("paged", lens, 4096, seed=13)
-    assert api.dr_plan_splits(1, 16, 4096, 152) == api.dr_plan_splits(96, 16, 4096, 152) == 8
+    bf16 = api.DR_KV_BF16
+    assert api.dr_plan_splits(1, 16, 4096, bf16, 152) == api.dr_plan_splits(8, 16, 4096, bf16, 152) == 8
     kv = to_dev(cache, dev)
     seq = torch.from_numpy(w.seq_len).to(dev)
     big = torch.empty((w.B, 16, D), dtype=torch.float32, device=dev)

@@ -147,8 +147,8 @@ def test_fused_layer_cross_row_layouts(api, cuda_device, B, self_len, enc_max):
     enc_len = rng.integers(1, enc_max, size=B, endpoint=True).astype(np.int32)
     w = W.Workload(130 + B, "layouts", 1, B, "paged", lens, 4096, enc_len, enc_max, 1.0, 1, 1.0,
                    np.zeros(B, np.uint64), np.zeros(B, np.int32))
-    s_self = api.dr_plan_splits(B, 16, int(lens.max()), 152)
-    s_cross = api.dr_plan_splits(B, 16, enc_max, 152)
+    s_self = api.dr_plan_splits(B, 16, int(lens.max()), api.DR_KV_BF16, 152)
+    s_cross = api.dr_plan_splits(B, 16, enc_max, api.DR_KV_BF16, 152)
     cache = W.make_self_cache(w, 0)
     q, qx, kn, vn = W.make_step_inputs(w, 0)
     kx, vx = W.make_cross_kv(w, 0)
@@ -167,4 +167,4 @@ def test_fused_layer_cross_row_layouts(api, cuda_device, B, self_len, enc_max):
     assert_attn_close(out, oracle.attn_paged(W.bits(q), kh, vh, t, lens, default_scale(D)),
                       f"self (splits {s_self})")
     assert_attn_close(outx, oracle.attn_contiguous(W.bits(qx), W.bits(kx), W.bits(vx), enc_len, default_scale(D)),
-                      f"cross (standalone plan {s_cross}, {'packed' if s_cross == 1 else 'split'})")
+                      f"cross (standalone plan {s_cross}, self plan {s_self})")
