@@ -224,14 +224,17 @@ class DeviceStep:
     def launches_per_step(self) -> int:
         return (1 if self.fused else 3) * self.w.layers + 1
 
-    def run_layer(self, l):
+    def run_layer(self, l, seq=None, pos=None):
+        """Layer l of the step; seq/pos (device int32 [B]) default to the workload's lengths."""
         api, L = self.api, self.layers[l]
+        seq = self.seq if seq is None else seq
+        pos = self.pos if pos is None else pos
         if self.fused:
-            api.dr_decode_layer(L["q"], L["kv"], L["kn"], L["vn"], self.seq, L["qx"], L["kx"], L["vx"], self.enc,
+            api.dr_decode_layer(L["q"], L["kv"], L["kn"], L["vn"], seq, L["qx"], L["kx"], L["vx"], self.enc,
                                 self.out_s[l], self.out_x[l], max_seq_len_hint=self.hint, err_flag=self.err)
         else:
-            api.dr_kv_append(L["kv"], L["kn"], L["vn"], self.pos, err_flag=self.err)
-            api.dr_decode_self_attn(L["q"], L["kv"], self.seq, self.out_s[l], max_seq_len_hint=self.hint,
+            api.dr_kv_append(L["kv"], L["kn"], L["vn"], pos, err_flag=self.err)
+            api.dr_decode_self_attn(L["q"], L["kv"], seq, self.out_s[l], max_seq_len_hint=self.hint,
                                     err_flag=self.err)
             api.dr_decode_cross_attn(L["qx"], L["kx"], L["vx"], self.enc, self.out_x[l], err_flag=self.err)
 
@@ -253,6 +256,49 @@ class DeviceStep:
         for l in range(self.w.layers):
             self.run_layer(l)
         self.run_sampler_only()
+
+
+def time_long_output(ds: DeviceStep, kv_bytes: int, chunk: int = 128) -> dict:
+    """The long-output run itself (batch 1): n_steps consecutive steps, step t appending key t of every layer,
+    attending t + 1 keys and sampling with the device step counter advancing.  Captured as graphs of `chunk`
+    steps (the lengths come from a device array, one element per step) and replayed back to back between two
+    events.  Overwrites the caches' first n_steps keys."""
+    w, api, dev = ds.w, ds.api, ds.dev
+    assert w.B == 1 and w.n_steps > 1
+    T = w.n_steps
+    lens = torch.arange(1, T + 1, dtype=torch.int32, device=dev)
+    step = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    pos_all = lens - 1   # the separate append call reads its position from here
+    graphs = []
+    for t0 in range(0, T, chunk):
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream()
+        cs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cs):
+            for t in range(t0, min(T, t0 + chunk)):
+                for l in range(w.layers):
+                    ds.run_layer(l, seq=lens[t:t + 1], pos=pos_all[t:t + 1])
+                api.dr_sample_topk_delayed(ds.logits, w.temperature, w.top_k, ds.seeds, step, w.pad_id, ds.tokens,
+                                           V=w.V, advance=True)
+        torch.cuda.current_stream().wait_stream(cs)
+        graphs.append(g)
+    for g in graphs:                                          # untimed pass: first-touch costs
+        g.replay()
+    torch.cuda.synchronize()
+    step.zero_()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for g in graphs:
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    total_ms = e0.elapsed_time(e1)
+    total_bytes = sum(step_bytes(dataclasses.replace(w, seq_len=np.array([t + 1], np.int32)), kv_bytes=kv_bytes)["step"]
+                      for t in range(T))
+    return {"steps": T, "mean_us_per_step": total_ms * 1e3 / T, "GBps": total_bytes / (total_ms * 1e-3) / 1e9,
+            "launches": T * ds.launches_per_step(),
+            "timing": f"{len(graphs)} graphs of {chunk} steps replayed back to back, events around them"}
 
 
 class HostStep:
@@ -517,6 +563,10 @@ def main():
                "h2d_bytes_per_step": hs.h2d, "d2h_bytes_per_step": hs.d2h,
                "mode": "cuda_graph with copy nodes" if g_e2e is not None else "eager"}
 
+    # the long-output workload: also the whole growing run, not only its last (longest) step
+    long_output = time_long_output(ds, kv_bytes=1 if args.kv == "fp8" else 2) \
+        if w.n_steps > 1 and not args.eager else None
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         r = time_oracle(w, 1, min_seconds=10.0)
@@ -540,6 +590,8 @@ def main():
                 "kernel_timing": "dominant kernel and sampler: K x layers (K) launches of the timed steps, "
                                  "back to back in their own graph, events around it",
                 "clocks": clk.summary()}
+        if long_output is not None:
+            line["long_output"] = long_output
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
