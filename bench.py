@@ -47,6 +47,9 @@ NOMINAL_HBM_GBS = 8000.0
 # ---------------------------------------------------------------------------
 # bytes the step must move (algorithmic, not measured)
 # ---------------------------------------------------------------------------
+HEAD_COPIES = 8   # distinct LM-head weight / embedding-table copies: 8 x 20 MB, more than the 129 MB L2
+
+
 def step_bytes(w: W.Workload, out_bytes: int = 2, kv_bytes: int = 2):
     """Bytes one decode step must move; kv_bytes is the self cache's element size (2 bf16, 1 e4m3)."""
     BHD = w.B * w.H * w.D
@@ -208,18 +211,22 @@ class DeviceStep:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.hint = int(w.seq_len.max())
         # the decoder's output and input ends (not part of the timed step): merged LM head and
-        # merged embedding lookup, synthetic weights [C*V, 1024] bf16
+        # merged embedding lookup, synthetic weights [C*V, 1024] bf16.  HEAD_COPIES distinct copies of
+        # each (160 MB in all, more than L2) are used in turn, so every call reads its weights from HBM.
         self.hidden = W.randn_bf16((w.B, 1024), dev, w.index, 500 + rank)
-        self.w_head = (W.randn_bf16((w.C * w.V, 1024), dev, w.index, 501) * 0.1).contiguous()
-        self.w_emb = W.randn_bf16((w.C * w.V, 1024), dev, w.index, 502)
+        self.w_head = [(W.randn_bf16((w.C * w.V, 1024), dev, w.index, 501 + 2 * i) * 0.1).contiguous()
+                       for i in range(HEAD_COPIES)]
+        self.w_emb = [W.randn_bf16((w.C * w.V, 1024), dev, w.index, 502 + 2 * i) for i in range(HEAD_COPIES)]
         self.head_logits = torch.empty((w.B, w.C, w.ldv), dtype=torch.float32, device=dev)
         self.emb_out = torch.empty((w.B, 1024), dtype=torch.bfloat16, device=dev)
 
-    def run_lm_head(self):
-        self.api.dr_lm_head(self.hidden, self.w_head, self.w.C, self.head_logits, err_flag=self.err)
+    def run_lm_head(self, i: int = 0):
+        self.api.dr_lm_head(self.hidden, self.w_head[i % HEAD_COPIES], self.w.C, self.head_logits,
+                            err_flag=self.err)
 
-    def run_embed(self):
-        self.api.dr_embed_tokens(self.tokens, self.w_emb, self.w.V, self.emb_out, err_flag=self.err)
+    def run_embed(self, i: int = 0):
+        self.api.dr_embed_tokens(self.tokens, self.w_emb[i % HEAD_COPIES], self.w.V, self.emb_out,
+                                 err_flag=self.err)
 
     def launches_per_step(self) -> int:
         return (1 if self.fused else 3) * self.w.layers + 1
@@ -493,12 +500,12 @@ def main():
             ds.run_sampler_only()
 
     def head_only():
-        for _ in range(K):
-            ds.run_lm_head()
+        for i in range(K):
+            ds.run_lm_head(i)
 
     def embed_only():
-        for _ in range(K):
-            ds.run_embed()
+        for i in range(K):
+            ds.run_embed(i)
 
     regions = {"step": steps, "self": self_only, "sampler": sampler_only, "lm_head": head_only, "embed": embed_only}
     graphs = {k: capture(f) for k, f in regions.items()} if not args.eager else None
@@ -584,8 +591,10 @@ def main():
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "decoder_ends": {
                     "lm_head": {"us": head_total_ms / K * 1e3, "batch": w.B, "K": 1024, "N": w.C * w.V,
-                                "weight_GBps": w.C * w.V * 1024 * 2 / (head_total_ms / K * 1e-3) / 1e9},
-                    "embed": {"us": emb_total_ms / K * 1e3, "rows_gathered": w.B * w.C, "Dm": 1024}},
+                                "weight_GBps": w.C * w.V * 1024 * 2 / (head_total_ms / K * 1e-3) / 1e9,
+                                "weights": f"{HEAD_COPIES} copies used in turn (more than L2)"},
+                    "embed": {"us": emb_total_ms / K * 1e3, "rows_gathered": w.B * w.C, "Dm": 1024,
+                              "tables": f"{HEAD_COPIES} copies used in turn (more than L2)"}},
                 "gpu_launches": ds.launches_per_step() * K, "launch_mode": mode,
                 "kernel_timing": "dominant kernel and sampler: K x layers (K) launches of the timed steps, "
                                  "back to back in their own graph, events around it",

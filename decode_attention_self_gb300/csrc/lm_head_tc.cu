@@ -5,20 +5,31 @@
 //
 //   logits^T[n, b] = sum_k W[n, k] * hidden[b, k]       (n = c*V + v)
 //
-// One CTA computes a 128-row slab of W against a tile of up to 256 batch rows:
-// the weight slab is the MMA's M = 128 operand A, the batch tile its N operand
-// B, both K-major bf16 in shared memory with the 128-byte swizzle, and the fp32
-// accumulator lives in tensor memory (128 lanes x N columns).
+// One CTA computes a 128-row slab of W against a tile of up to 128 batch rows
+// over its share of K: the weight slab is the MMA's M = 128 operand A, the batch
+// tile its N operand B, both K-major bf16 in shared memory with the 128-byte
+// swizzle, and the fp32 accumulator lives in tensor memory (128 lanes x N
+// columns).
 //   warp 0, lane 0 : TMA producer -- cp.async.bulk.tensor.2d loads of 64-wide K
-//                    chunks of A and B into a 4-stage ring, completion counted
+//                    chunks of A and B into a ring of up to 4 stages, completion counted
 //                    on the stage's "full" mbarrier;
 //   warp 1, lane 0 : MMA issuer -- four tcgen05.mma (K = 16 each) per chunk,
 //                    tcgen05.commit to the stage's "empty" mbarrier, and a last
 //                    commit to "done";
 //   all 4 warps    : epilogue -- warp w reads TMEM lanes 32w..32w+31 with
 //                    tcgen05.ld and writes fp32 logits into the sampler layout.
-// Every wait is bounded: a wait that runs out sets DR_ERRF_TIMEOUT and the CTA
-// skips the rest of its work (a correct launch never gets there).
+// Split K (batch tiles of up to 32 rows): when the weight slabs alone are fewer
+// than the SMs, K is cut in two and the two CTAs of a cluster each accumulate
+// one half.  Each stages the half of its partial accumulator that the other
+// owns in its (then idle) stage ring; after a cluster barrier each CTA adds the
+// two partials for its own batch columns, rank 0's first, reading the other's
+// through distributed shared memory.  Whenever the grid has more CTAs than the
+// GPU has SMs, the ring is cut to at most 112 KB so that two CTAs share an SM
+// and the grid runs as one wave.
+// Every mbarrier wait is bounded: a wait that runs out sets DR_ERRF_TIMEOUT
+// and the CTA skips the rest of its work (a correct launch never gets there);
+// both cluster barriers are reached on every path.
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -31,8 +42,10 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kTileN = 128;          // W rows per CTA (MMA M)
 constexpr int kChunkK = 64;          // K elements per stage: one 128-byte swizzled row
-constexpr int kStages = 4;
-constexpr int kMaxBatchTile = 256;   // MMA N limit
+constexpr int kMaxStages = 4;
+constexpr int kTwoPerSmBytes = 112 * 1024;   // stage ring small enough for two CTAs per SM
+constexpr int kMaxBatchTile = 128;   // MMA N (a multiple of 16); larger batches take more tiles
+constexpr int kMaxSplitK = 2;
 constexpr long long kWaitLimit = 4LL << 30;   // clock cycles (about 2 s)
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -97,41 +110,70 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                  : "memory");
 }
 
+// tcgen05.ld of 32 (or 8) consecutive fp32 accumulator columns starting at
+// column c0, TMEM lanes 32w .. 32w+31 (one row per thread of warp w).
+__device__ __forceinline__ void tmem_ld32(uint32_t tmem, int warp, int c0, uint32_t (&r)[32]) {
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t tmem, int warp, int c0, uint32_t (&r)[8]) {
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 struct TcParams {
     float *logits;     // [B][C][ldv]
     int32_t B, K, C, V, ldv, btile, tmem_cols;
+    int32_t ksplit;    // CTAs (one cluster along x) that share a weight slab's K range
+    int32_t stages;    // depth of the stage ring, <= kMaxStages
     int32_t *err;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     lm_head_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
                       const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t full[kStages], empty[kStages], done;
+    __shared__ uint64_t full[kMaxStages], empty[kMaxStages], done;
     __shared__ uint32_t tmem_base;
-    __shared__ int abort_flag;
+    __shared__ int abort_flag, cta_ok;
 
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kTileN;
+    const int ks = p.ksplit;
+    const int kpart = (int)blockIdx.x % ks;   // rank in the cluster
+    const int n0 = ((int)blockIdx.x / ks) * kTileN;
     const int b0 = blockIdx.y * p.btile;
     const int N = p.C * p.V;
-    const int chunks = p.K / kChunkK;
+    const int chunks = p.K / kChunkK / ks;
+    const int kc0 = kpart * chunks;
     const uint32_t bytes_a = kTileN * kChunkK * 2;
     const uint32_t bytes_b = (uint32_t)p.btile * kChunkK * 2;
 
     // 1024-byte aligned stage ring: A stages, then B stages
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sa = base;
-    uint8_t *sb = base + kStages * bytes_a;
+    uint8_t *sb = base + p.stages * bytes_a;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         mbar_init(&done, 1);
         abort_flag = 0;
+        cta_ok = 1;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -145,25 +187,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_base;
 
     if (warp == 0 && lane == 0) {
-        // producer
-        for (int kc = 0; kc < chunks; ++kc) {
-            const int s = kc % kStages;
-            if (kc >= kStages && !mbar_wait(&empty[s], ((kc / kStages) - 1) & 1)) {
+        // producer: stage s of round `round` (parity round & 1) waits for the MMAs of round - 1
+        for (int kc = 0, s = 0, round = 0; kc < chunks; ++kc) {
+            if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1)) {
                 abort_flag = 1;
                 flag_error(p.err, DR_ERRF_TIMEOUT);
                 break;
             }
             mbar_expect_tx(&full[s], bytes_a + bytes_b);
-            tma_load_2d(sa + s * bytes_a, &map_w, kc * kChunkK, n0, &full[s]);
-            tma_load_2d(sb + s * bytes_b, &map_h, kc * kChunkK, b0, &full[s]);
+            tma_load_2d(sa + s * bytes_a, &map_w, (kc0 + kc) * kChunkK, n0, &full[s]);
+            tma_load_2d(sb + s * bytes_b, &map_h, (kc0 + kc) * kChunkK, b0, &full[s]);
+            if (++s == p.stages) {
+                s = 0;
+                ++round;
+            }
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer
         const uint32_t idesc = instr_desc(kTileN, p.btile);
         bool ok = true;
-        for (int kc = 0; kc < chunks; ++kc) {
-            const int s = kc % kStages;
-            if (!mbar_wait(&full[s], (kc / kStages) & 1)) {
+        for (int kc = 0, s = 0, round = 0; kc < chunks; ++kc) {
+            if (!mbar_wait(&full[s], round & 1)) {
                 ok = false;
                 break;
             }
@@ -175,6 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_bf16(tmem, a, b, idesc, (kc | k) != 0);
             }
             mma_commit(&empty[s]);   // the stage is free once these MMAs have read it
+            if (++s == p.stages) {
+                s = 0;
+                ++round;
+            }
         }
         if (!ok) {
             abort_flag = 1;
@@ -190,30 +238,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (!finished) {
         if (lane == 0) flag_error(p.err, DR_ERRF_TIMEOUT);
-    } else if (!abort_flag) {
-        const int n = n0 + warp * 32 + lane;
-        const int c = n / p.V, v = n - c * p.V;
-        for (int c0 = 0; c0 < p.btile; c0 += 32) {
-            uint32_t r[32];
-            const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0;
-            asm volatile(
-                "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-                "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                  "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-                  "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-                  "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-                  "=r"(r[30]), "=r"(r[31])
-                : "r"(taddr));
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            if (n < N) {
+        cta_ok = 0;
+    }
+    const int row = warp * 32 + lane;
+    const int n = n0 + row;
+    const int c = n / p.V, v = n - c * p.V;
+    const bool have = finished && !abort_flag;
+    if (ks == 1) {
+        if (have)
+            for (int c0 = 0; c0 < p.btile; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem, warp, c0, r);
+                if (n < N) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int b = b0 + c0 + j;
-                    if (b < p.B) p.logits[((size_t)b * p.C + c) * p.ldv + v] = __uint_as_float(r[j]);
+                    for (int j = 0; j < 32; ++j) {
+                        const int b = b0 + c0 + j;
+                        if (b < p.B) p.logits[((size_t)b * p.C + c) * p.ldv + v] = __uint_as_float(r[j]);
+                    }
                 }
             }
-        }
+    } else {
+        // Two CTAs: this one owns batch columns [kpart * half, (kpart + 1) * half).  It stages the
+        // other half of its partial, [column][128 rows] fp32, in its idle stage ring for the peer.
+        const int half = p.btile / 2;   // a multiple of 8
+        const int own0 = kpart * half, other0 = (kpart ^ 1) * half;
+        float *staged = reinterpret_cast<float *>(base);
+        if (have)
+            for (int c0 = 0; c0 < half; c0 += 8) {
+                uint32_t r[8];
+                tmem_ld8(tmem, warp, other0 + c0, r);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) staged[(c0 + j) * kTileN + row] = __uint_as_float(r[j]);
+            }
+        cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+        cluster.sync();   // both partials (and both CTAs' status) are staged and visible
+        const unsigned peer = (unsigned)(kpart ^ 1);
+        const bool peer_ok = *cluster.map_shared_rank(&cta_ok, peer) != 0 &&
+                             *cluster.map_shared_rank(&abort_flag, peer) == 0;
+        const float *theirs = cluster.map_shared_rank(staged, peer);
+        if (have && peer_ok)
+            for (int c0 = 0; c0 < half; c0 += 8) {
+                uint32_t r[8];
+                tmem_ld8(tmem, warp, own0 + c0, r);
+                float t[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) t[j] = theirs[(c0 + j) * kTileN + row];   // 8 loads in flight
+                if (n < N) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int b = b0 + own0 + c0 + j;
+                        // rank 0's partial first
+                        const float sum = kpart == 0 ? __uint_as_float(r[j]) + t[j] : t[j] + __uint_as_float(r[j]);
+                        if (b < p.B) p.logits[((size_t)b * p.C + c) * p.ldv + v] = sum;
+                    }
+                }
+            }
+        cluster.sync();   // keep the staged halves alive until both CTAs have read them
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -250,7 +330,7 @@ bool encode_2d(CUtensorMap *map, const void *ptr, int rows, int K, int box_rows)
 
 }  // namespace
 
-// Batch rows per CTA tile: a multiple of 16 (the MMA's N granularity), at most 256.
+// Batch rows per CTA tile: a multiple of 16 (the MMA's N granularity), at most 128.
 int lm_head_tc_batch_tile(int B) {
     int t = ((B + 15) / 16) * 16;
     return t > kMaxBatchTile ? kMaxBatchTile : t;
@@ -270,15 +350,25 @@ cudaError_t launch_lm_head_tc(const LmHeadParams &p, int32_t *err, cudaStream_t 
     while (cols < tp.btile) cols <<= 1;
     tp.tmem_cols = cols;
     tp.err = err;
+    const int mtiles = (N + kTileN - 1) / kTileN;
+    const int ntiles = (p.B + tp.btile - 1) / tp.btile;
+    const int sms = current_device_sms();
+    // Split K in two for small batch tiles when the weight slabs alone leave SMs idle; with more CTAs
+    // than SMs the ring shrinks so that two CTAs share an SM (one wave).
+    tp.ksplit = (tp.btile <= 32 && mtiles * ntiles <= sms && (p.K / kChunkK) % kMaxSplitK == 0) ? kMaxSplitK : 1;
+    const int stage_bytes = (kTileN + tp.btile) * kChunkK * 2;
+    tp.stages = mtiles * ntiles * tp.ksplit > sms ? kTwoPerSmBytes / stage_bytes : kMaxStages;
+    if (tp.stages > kMaxStages) tp.stages = kMaxStages;
     CUtensorMap map_w, map_h;
     if (!encode_2d(&map_w, p.W, N, p.K, kTileN) || !encode_2d(&map_h, p.hidden, p.B, p.K, tp.btile))
         return cudaErrorInvalidValue;
-    const size_t smem = 1024 + (size_t)kStages * (kTileN + tp.btile) * kChunkK * 2;
+    const size_t smem = 1024 + (size_t)tp.stages * stage_bytes;
     const cudaError_t e = cudaFuncSetAttribute(lm_head_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((N + kTileN - 1) / kTileN), (unsigned)((p.B + tp.btile - 1) / tp.btile));
-    return launch_kernel(lm_head_tc_kernel, grid, dim3(kThreads), smem, stream, 1u, map_w, map_h, tp);
+    dim3 grid((unsigned)(mtiles * tp.ksplit), (unsigned)ntiles);
+    return launch_kernel(lm_head_tc_kernel, grid, dim3(kThreads), smem, stream, (unsigned)tp.ksplit, map_w, map_h,
+                         tp);
 }
 
 }  // namespace dr
