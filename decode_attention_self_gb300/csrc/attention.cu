@@ -19,7 +19,9 @@
 //   512 contiguous bytes.  Each lane group keeps an fp32 online-softmax state
 //   (running max m, running sum l, acc[8]); states are merged with warp
 //   shuffles, then across warps in shared memory, then across the cluster's
-//   CTAs through distributed shared memory by CTA rank 0.
+//   CTAs: each CTA writes its state into CTA rank 0's shared memory
+//   (distributed shared memory), and rank 0 merges them after one cluster
+//   barrier.
 //
 // Roofline: a key costs 256 bytes (64 bf16 of K and of V) and ~260 flops, so
 // the kernel is bound by HBM bandwidth; there is no dense contraction for the
@@ -41,6 +43,7 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kD = kHeadDim;
 constexpr int kTile = kBlockKeys;
+constexpr int kMaxSplits = 8;   // CTAs per row: one portable cluster
 
 struct SoftmaxPartial {
     float m;         // max of scaled log2-domain scores
@@ -318,7 +321,7 @@ template <typename KV, bool kPaged, bool kPipelined, bool kFused>
 __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kernel(const AttnParams p) {
     __shared__ float s_wm[kWarps], s_wl[kWarps];
     __shared__ float s_wacc[kWarps][kD];
-    __shared__ SoftmaxPartial s_part;
+    __shared__ SoftmaxPartial s_parts[kMaxSplits];   // rank 0 of a cluster collects the CTAs' states here
 
     pdl_wait();
     const int h = blockIdx.y;
@@ -372,12 +375,18 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     const float out_scale = cross ? 1.0f : p.out_scale;
 
     __syncthreads();
-    if (threadIdx.x < kD) {
-        const int d = threadIdx.x;
-        float mm = -INFINITY;
+    void *outp = cross ? p.xout : p.out;
+    const int d = threadIdx.x;   // threads d < kD each own output dim d
+    const size_t oidx = row * kD + d;
+    auto store = [&](float o) {
+        if (p.out_f32) reinterpret_cast<float *>(outp)[oidx] = o;
+        else reinterpret_cast<uint16_t *>(outp)[oidx] = f32_to_bf16_rn(o);
+    };
+    // CTA merge of the warps' states (m and l come out the same in every thread)
+    float mm = -INFINITY, ls = 0.f, o = 0.f;
+    if (d < kD) {
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, s_wm[w]);
-        float ls = 0.f, o = 0.f;
         if (mm != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) {
@@ -386,52 +395,39 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
                 o += wt * s_wacc[w][d];
             }
         }
-        s_part.acc[d] = o;
-        if (d == 0) {
-            s_part.m = mm;
-            s_part.l = ls;
-        }
     }
-
-    void *outp = cross ? p.xout : p.out;
-    float *out_f = reinterpret_cast<float *>(outp) + row * kD;
-    uint16_t *out_h = reinterpret_cast<uint16_t *>(outp) + row * kD;
-
-    if (nsplit == 1) {
-        __syncthreads();
-        if (threadIdx.x < kD) {
-            const int d = threadIdx.x;
-            const float o = s_part.l > 0.f ? s_part.acc[d] / s_part.l * out_scale : 0.f;
-            if (p.out_f32) out_f[d] = o;
-            else out_h[d] = f32_to_bf16_rn(o);
-        }
+    if (nsplit == 1) {   // the same for every CTA of a cluster
+        if (d < kD) store(ls > 0.f ? o / ls * out_scale : 0.f);
         return;
     }
 
-    // Cluster-wide merge of the S partial states (CTA rank == split).
+    // Cluster merge: every CTA pushes its state into slot `split` of rank 0's shared memory, then one
+    // cluster barrier, which every thread of the cluster reaches (release / acquire), makes all of them
+    // visible to rank 0.  Nothing reads another CTA's shared memory after the barrier, so the other CTAs
+    // may exit at once.
     cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();   // every CTA's s_part is complete and visible
-    if (split == 0 && threadIdx.x < kD) {
-        const int d = threadIdx.x;
-        float mm = -INFINITY;
-        for (int r = 0; r < nsplit; ++r) {
-            const SoftmaxPartial *pr = cluster.map_shared_rank(&s_part, r);
-            mm = fmaxf(mm, pr->m);
+    if (d < kD) {
+        SoftmaxPartial *slot = cluster.map_shared_rank(&s_parts[split], 0);
+        slot->acc[d] = o;
+        if (d == 0) {
+            slot->m = mm;
+            slot->l = ls;
         }
-        float ls = 0.f, o = 0.f;
-        if (mm != -INFINITY) {
-            for (int r = 0; r < nsplit; ++r) {
-                const SoftmaxPartial *pr = cluster.map_shared_rank(&s_part, r);
-                const float wt = exp2f(pr->m - mm);
-                ls += wt * pr->l;
-                o += wt * pr->acc[d];
-            }
-        }
-        o = ls > 0.f ? o / ls * out_scale : 0.f;
-        if (p.out_f32) out_f[d] = o;
-        else out_h[d] = f32_to_bf16_rn(o);
     }
-    cluster.sync();   // keep every CTA's shared memory alive until rank 0 has read it
+    cluster.sync();
+    if (split != 0 || d >= kD) return;
+    mm = -INFINITY;
+    for (int r = 0; r < nsplit; ++r) mm = fmaxf(mm, s_parts[r].m);
+    ls = 0.f;
+    o = 0.f;
+    if (mm != -INFINITY) {
+        for (int r = 0; r < nsplit; ++r) {
+            const float wt = exp2f(s_parts[r].m - mm);
+            ls += wt * s_parts[r].l;
+            o += wt * s_parts[r].acc[d];
+        }
+    }
+    store(ls > 0.f ? o / ls * out_scale : 0.f);
 }
 
 template <typename KV, bool kPaged, bool kPipelined, bool kFused>
@@ -439,10 +435,7 @@ cudaError_t launch_variant(const AttnParams &p, int splits, cudaStream_t stream)
     unsigned zrows = (unsigned)p.B;
     if (kFused && p.xq) zrows += p.xpacked ? (unsigned)((p.B + splits - 1) / splits) : (unsigned)p.B;
     auto kern = decode_attn_kernel<KV, kPaged, kPipelined, kFused>;
-    if (splits > 8) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
+    if (splits < 1 || splits > kMaxSplits) return cudaErrorInvalidValue;   // rank 0 has kMaxSplits slots
     return launch_kernel(kern, dim3((unsigned)splits, (unsigned)p.H, zrows), dim3(kThreads), 0, stream,
                          (unsigned)splits, p);
 }
