@@ -312,6 +312,55 @@ __device__ __forceinline__ void attend_range(const AttnParams &p, bool cross_row
     }
 }
 
+__device__ __forceinline__ int ld_relaxed(const int32_t *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// L2 prefetch of the K and V rows of warp `warp`'s first two tiles, issued
+// before the kernel waits for its predecessor on the stream.  Only a hint: the
+// length and the block table may still be changing (the predecessor may write
+// them), so they are read with relaxed loads, every address is checked against
+// the row's capacity or the block pool, and the real loads after the wait use
+// the final values.  L2 is coherent with the predecessor's writes.
+template <typename KV, bool kPaged>
+__device__ __forceinline__ void prefetch_first_tiles(const AttnParams &p, bool cross, int b, int h, int split,
+                                                     int nsplit, int warp) {
+    constexpr uint32_t kRowBytes = (uint32_t)kD * KV::kElemBytes;
+    const int cap = cross ? p.xcap : p.cap;
+    int L = ld_relaxed((cross ? p.xlens : p.lens) + b);
+    L = L < 0 ? 0 : (L > cap ? cap : L);
+    const int ntiles = (L + kTile - 1) / kTile;
+    const int per = (ntiles + nsplit - 1) / nsplit;
+    const int key0 = min(split * per, ntiles) * kTile;
+    const int key1 = min(key0 + per * kTile, L);
+    const uint8_t *kc = reinterpret_cast<const uint8_t *>(cross ? p.xk : p.k);
+    const uint8_t *vc = reinterpret_cast<const uint8_t *>(cross ? p.xv : p.v);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int t = key0 + (warp + i * kWarps) * kTile;
+        if (t >= key1) break;
+        size_t base;
+        uint32_t bytes;
+        if (kPaged) {
+            const int blk = ld_relaxed(p.table + (size_t)b * p.max_blocks + t / kTile);
+            if ((unsigned)blk >= (unsigned)p.num_blocks) break;
+            base = ((size_t)blk * p.H + h) * kTile * kRowBytes;
+            bytes = kTile * kRowBytes;
+        } else {
+            base = (((size_t)b * p.H + h) * (size_t)cap + (size_t)t) * kRowBytes;
+            bytes = (uint32_t)min(kTile, cap - t) * kRowBytes;
+        }
+        prefetch_l2(kc + base, bytes);
+        prefetch_l2(vc + base, bytes);
+    }
+}
+
 // kPipelined: each warp keeps the next tile's loads in flight while it
 // computes the current one (twice the bytes in flight per warp, at ~100
 // registers instead of 64).  Chosen when the whole grid is resident at once,
@@ -323,7 +372,6 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     __shared__ float s_wacc[kWarps][kD];
     __shared__ SoftmaxPartial s_parts[kMaxSplits];   // rank 0 of a cluster collects the CTAs' states here
 
-    pdl_wait();
     const int h = blockIdx.y;
     // Fused launches carry the B self rows along z, then the cross rows: split
     // like the self rows (z = B + b), or packed one row per CTA (row b =
@@ -337,6 +385,13 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     if (b >= p.B) return;   // tail of the packed region (no cluster barrier is reached there)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+
+    // While the previous kernel on the stream drains, warm L2 with this warp's first tiles; then wait for it.
+    if (lane == 0) {
+        if (cross) prefetch_first_tiles<Bf16Kv, false>(p, true, b, h, split, nsplit, warp);
+        else prefetch_first_tiles<KV, kPaged>(p, false, b, h, split, nsplit, warp);
+    }
+    pdl_wait();
 
     const size_t row = (size_t)b * p.H + h;
     const int cap = cross ? p.xcap : p.cap;
