@@ -322,13 +322,15 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// L2 prefetch of the K and V rows of warp `warp`'s first two tiles, issued
-// before the kernel waits for its predecessor on the stream.  Only a hint: the
+// L2 prefetch of the K and V rows of warp `warp`'s first kPrefetchTiles tiles
+// (the pipelined variant, whose whole grid is resident at once, prefetches its
+// whole range; the streaming variant its first two tiles), issued before the
+// kernel waits for its predecessor on the stream.  Only a hint: the
 // length and the block table may still be changing (the predecessor may write
 // them), so they are read with relaxed loads, every address is checked against
 // the row's capacity or the block pool, and the real loads after the wait use
 // the final values.  L2 is coherent with the predecessor's writes.
-template <typename KV, bool kPaged>
+template <typename KV, bool kPaged, int kPrefetchTiles>
 __device__ __forceinline__ void prefetch_first_tiles(const AttnParams &p, bool cross, int b, int h, int split,
                                                      int nsplit, int warp) {
     constexpr uint32_t kRowBytes = (uint32_t)kD * KV::kElemBytes;
@@ -341,8 +343,7 @@ __device__ __forceinline__ void prefetch_first_tiles(const AttnParams &p, bool c
     const int key1 = min(key0 + per * kTile, L);
     const uint8_t *kc = reinterpret_cast<const uint8_t *>(cross ? p.xk : p.k);
     const uint8_t *vc = reinterpret_cast<const uint8_t *>(cross ? p.xv : p.v);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kPrefetchTiles; ++i) {
         const int t = key0 + (warp + i * kWarps) * kTile;
         if (t >= key1) break;
         size_t base;
@@ -386,10 +387,10 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // While the previous kernel on the stream drains, warm L2 with this warp's first tiles; then wait for it.
+    // While the previous kernel on the stream drains, warm L2 with this warp's tiles; then wait for it.
     if (lane == 0) {
-        if (cross) prefetch_first_tiles<Bf16Kv, false>(p, true, b, h, split, nsplit, warp);
-        else prefetch_first_tiles<KV, kPaged>(p, false, b, h, split, nsplit, warp);
+        if (cross) prefetch_first_tiles<Bf16Kv, false, kPipelined ? 64 : 2>(p, true, b, h, split, nsplit, warp);
+        else prefetch_first_tiles<KV, kPaged, kPipelined ? 64 : 2>(p, false, b, h, split, nsplit, warp);
     }
     pdl_wait();
 
