@@ -312,16 +312,6 @@ __device__ __forceinline__ void attend_range(const AttnParams &p, bool cross_row
     }
 }
 
-__device__ __forceinline__ int ld_relaxed(const int32_t *p) {
-    int v;
-    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // L2 prefetch of the K and V rows of warp `warp`'s first kPrefetchTiles tiles
 // (the pipelined variant, whose whole grid is resident at once, prefetches its
 // whole range; the streaming variant its first two tiles), issued before the

@@ -84,6 +84,20 @@ __device__ __forceinline__ void pdl_trigger() {
 #endif
 }
 
+// Relaxed (gpu scope) load: a value that another grid may still be writing,
+// read without a data race (used only for prefetch hints).
+__device__ __forceinline__ int ld_relaxed(const int32_t *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple
+// of 16).  A hint: it changes no data and L2 stays coherent with every writer.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void flag_error(int32_t *err, int bits) {
     if (err) atomicOr(err, bits);
 }

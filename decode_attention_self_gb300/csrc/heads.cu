@@ -76,12 +76,16 @@ constexpr int kBatch = 16;    // hidden vectors per shared-memory stage
 template <int KC>   // 16-byte chunks per lane per row: K = 256 * KC
 __global__ void __launch_bounds__(kHeadThreads) lm_head_kernel(const LmHeadParams p) {
     extern __shared__ uint4 s_hidden[];   // [kBatch][K/8]
-    pdl_wait();
-    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = (blockIdx.x * kHeadWarps + warp) * kRows;
     const int N = p.C * p.V;
     const int kchunks = 32 * KC;
+    // The weights are parameters, not an output of the previous kernel: warm L2 with this warp's rows
+    // (contiguous) while that kernel drains, then wait for it.
+    if (lane == 0 && n0 < N)
+        prefetch_l2(p.W + (size_t)n0 * (kchunks * 8), (uint32_t)(min(kRows, N - n0) * kchunks * 16));
+    pdl_wait();
+    pdl_trigger();
 
     uint4 wr[kRows][KC];
 #pragma unroll
