@@ -11,12 +11,15 @@
 //   1. reads its V logits once (element i = t + 256 j stays in thread t's
 //      registers), divides by T with IEEE round-to-nearest and maps each float
 //      to an order-preserving uint32 key;
-//   2. finds the top_k-th largest key tau by a 4-pass, 8-bit radix select:
-//      double-buffered shared-memory histograms (shared atomics), scanned in
-//      descending digit order, three barriers per pass;
-//   3. keeps every key > tau plus the lowest-index entries equal to tau (their
-//      rank in index order comes from warp ballots), so ties go to the lower
-//      index exactly, and compacts the kept indices into a shared list;
+//   2. finds the top_k-th largest key tau by an 8-bit radix select of up to 4
+//      passes: double-buffered shared-memory histograms (shared atomics), one
+//      warp scanning each in descending digit order, two barriers per pass.
+//      When the digit bin that holds the top_k-th key holds exactly the keys
+//      still needed, the whole bin is kept and the select stops there;
+//   3. keeps every key above the threshold plus, when the select ran to a full
+//      key, the lowest-index entries equal to tau (their rank in index order
+//      comes from warp ballots), so ties go to the lower index exactly, and
+//      compacts the kept indices into a shared list;
 //   4. draws by Gumbel-max over the list, spread evenly over the threads:
 //      u_i from Philox4x32-10 (Salmon et al., SC'11) keyed by the row's seed,
 //      counter (i/4, c, step, b); argmax of x_i - log(-log u_i), equal scores
@@ -98,7 +101,7 @@ template <int EPT>
 __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) {
     __shared__ uint32_t s_hist[2][256];
     __shared__ uint32_t s_wtot[kWarps];
-    __shared__ int s_sel[2];
+    __shared__ int s_sel[3];   // selected digit, keys still needed, keys in the digit's bin
     __shared__ uint32_t s_bal[EPT][kWarps];
     __shared__ int s_scan[kWarps];
     __shared__ int s_list[kMaxVocab];
@@ -139,6 +142,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) 
         // ---- radix select of the top_k-th largest key ------------------------
         uint32_t prefix = 0u, pmask = 0u;
         int kk = p.top_k;
+        bool whole_bin = false;   // the threshold bin is kept whole: no tie ranking needed
 #pragma unroll 1
         for (int pass = 0; pass < 4; ++pass) {
             const int shift = 24 - 8 * pass;
@@ -148,42 +152,60 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) 
                 if (((valid >> j) & 1u) && (key[j] & pmask) == prefix) atomicAdd(&hist[(key[j] >> shift) & 255u], 1u);
             }
             __syncthreads();
-            // thread t owns digit 255 - t: an inclusive scan over t walks digits downward
-            const uint32_t cnt = hist[255 - t];
-            uint32_t inc = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-                if (lane >= o) inc += n;
-            }
-            if (lane == 31) s_wtot[warp] = inc;
             s_hist[(pass + 1) & 1][t] = 0u;   // the other buffer is free: clear it for the next pass
-            __syncthreads();
-            uint32_t before = inc - cnt;
+            if (warp == 0) {
+                // lane l scans digits 255 - 8l down to 248 - 8l; a warp scan orders the lanes
+                uint32_t c8[8], sum = 0u;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w)
-                if (w < warp) before += s_wtot[w];
-            if (before < (uint32_t)kk && (uint32_t)kk <= before + cnt) {
-                s_sel[0] = 255 - t;
-                s_sel[1] = kk - (int)before;
+                for (int e = 0; e < 8; ++e) {
+                    c8[e] = hist[255 - 8 * lane - e];
+                    sum += c8[e];
+                }
+                uint32_t inc = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                    if (lane >= o) inc += n;
+                }
+                uint32_t before = inc - sum;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (before < (uint32_t)kk && (uint32_t)kk <= before + c8[e]) {
+                        s_sel[0] = 255 - 8 * lane - e;
+                        s_sel[1] = kk - (int)before;
+                        s_sel[2] = (int)c8[e];
+                    }
+                    before += c8[e];
+                }
             }
             __syncthreads();
             prefix |= (uint32_t)s_sel[0] << shift;
             pmask |= 0xFFu << shift;
             kk = s_sel[1];
+            if (kk == s_sel[2]) {   // the same in every thread
+                whole_bin = true;
+                break;
+            }
         }
-        const uint32_t tau = prefix;   // kk entries equal to tau are taken, lowest indices first
+        const uint32_t tau = prefix;   // without whole_bin: kk entries equal to tau are taken, lowest index first
 
-        // ---- membership: keys above tau, and the first kk ties in index order ----
-#pragma unroll
-        for (int j = 0; j < EPT; ++j) {
-            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ((valid >> j) & 1u) && key[j] == tau);
-            if (lane == 0) s_bal[j][warp] = bal;
-        }
-        __syncthreads();
+        // ---- membership: keys above the threshold, and ties in index order ------
         uint32_t member = 0u;
         int nmine = 0;
-        {
+        if (whole_bin) {
+#pragma unroll
+            for (int j = 0; j < EPT; ++j)
+                if (((valid >> j) & 1u) && (key[j] & pmask) >= prefix) {
+                    member |= 1u << j;
+                    ++nmine;
+                }
+        } else {
+#pragma unroll
+            for (int j = 0; j < EPT; ++j) {
+                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ((valid >> j) & 1u) && key[j] == tau);
+                if (lane == 0) s_bal[j][warp] = bal;
+            }
+            __syncthreads();
             const uint32_t lt_mask = (1u << lane) - 1u;
             int ties_before = 0;
 #pragma unroll
