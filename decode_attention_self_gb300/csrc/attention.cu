@@ -383,6 +383,10 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
         else prefetch_first_tiles<KV, kPaged, kPipelined ? 64 : 2>(p, false, b, h, split, nsplit, warp);
     }
     pdl_wait();
+    // The next kernel on the stream may start launching: at once when this grid is resident as a whole
+    // (its CTAs take free slots and prefetch), else once the streaming is done (below), so that they do
+    // not take the slots of this grid's later waves.
+    if (kPipelined) pdl_trigger();
 
     const size_t row = (size_t)b * p.H + h;
     const int cap = cross ? p.xcap : p.cap;
@@ -416,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
         attend_range<KV, kPaged, kPipelined, false, kSelfRows>(p, false, b, h, key0, key1, -1, warp, lane, s_wm, s_wl,
                                                               s_wacc);
     }
-    pdl_trigger();   // the streaming is done: the next kernel may start launching
+    if (!kPipelined) pdl_trigger();
     // an e4m3 value is code * v_scale: the kernel accumulates codes and scales the result
     const float out_scale = cross ? 1.0f : p.out_scale;
 

@@ -98,6 +98,17 @@ def test_planted_ties_at_the_topk_boundary(api, cuda_device):
     check(api, cuda_device, x, 0.7, k, np.arange(B, dtype=np.uint64) + 99, np.full(B, 15, np.int32), 1024)
 
 
+@pytest.mark.parametrize("k", [1, 2, 7, 50, 250, 1000, 1088])
+def test_few_distinct_values(api, cuda_device, k):
+    # Logits drawn from 12 distinct values, two of them equal in their first 16 bits: the bin of the
+    # top_k-th key often holds many equal keys, so the radix select ends at different passes, both with
+    # the bin kept whole and with the equal keys ranked by index.
+    rng = np.random.default_rng(k)
+    vals = np.array([-3.5, -1.25, -1.0, -0.5, 0.0, 0.125, 0.5, 1.0, 1.5, 2.0, 2.0078125, 4.0], np.float32)
+    logits = vals[rng.integers(0, len(vals), size=(6, 9, 1088))]
+    check(api, cuda_device, logits, 1.0, k, np.arange(6, dtype=np.uint64) + 11, np.full(6, 20, np.int32), 1024)
+
+
 def test_all_equal_logits_take_the_first_k(api, cuda_device):
     x = np.zeros((2, 9, 1088), np.float32)
     tok, pr, _ = run_gpu(api, cuda_device, x, 1.0, 50, np.array([1, 2], np.uint64), np.array([20, 20], np.int32), 5)
