@@ -309,31 +309,79 @@ def time_long_output(ds: DeviceStep, kv_bytes: int, chunk: int = 128) -> dict:
 
 
 class HostStep:
-    """End-to-end: the step's per-step inputs come from pinned host memory and its tokens go back to the host."""
+    """End to end: every step's inputs come from pinned host memory and its tokens go back to the host.
+
+    A step's inputs (every layer's q, q_cross, k_new, v_new, the logits, positions and lengths) are staged in
+    one pinned host buffer and move in one copy.  Inputs and drawn tokens are double-buffered on the device,
+    as a serving loop would do it: while step i runs on the compute stream, a copy stream reads back step
+    i - 1's tokens and brings step i + 1's inputs into the other buffer set (the one step i - 1 used, once
+    that step has finished).  Every copy and every token read-back is inside the timed region."""
+
+    KEYS = ("q", "qx", "kn", "vn")
 
     def __init__(self, ds: DeviceStep):
         self.ds = ds
-        self.h_in = []
-        for L in ds.layers:
-            self.h_in.append({k: L[k].cpu().pin_memory() for k in ("q", "qx", "kn", "vn")})
-        self.h_logits = ds.logits.cpu().pin_memory()
-        self.h_pos = ds.pos.cpu().pin_memory()
-        self.h_seq = ds.seq.cpu().pin_memory()
+        srcs = [(("layer", l, k), L[k]) for l, L in enumerate(ds.layers) for k in self.KEYS]
+        srcs += [(("logits",), ds.logits), (("pos",), ds.pos), (("seq",), ds.seq)]
+        offs, total = [], 0
+        for _, t in srcs:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256   # 256-byte aligned views
+        self.h_flat = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.sets = []
+        for _ in range(2):
+            flat = torch.empty(total, dtype=torch.uint8, device=ds.dev)
+            views = {}
+            for (name, t), o in zip(srcs, offs):
+                n = t.numel() * t.element_size()
+                views[name] = flat[o:o + n].view(t.dtype).view(t.shape)
+            self.sets.append({"flat": flat, "views": views, "tokens": torch.empty_like(ds.tokens)})
+        for (name, t), o in zip(srcs, offs):   # the host copy of the inputs
+            n = t.numel() * t.element_size()
+            self.h_flat[o:o + n].view(t.dtype).view(t.shape).copy_(t.cpu())
         self.h_tokens = torch.empty_like(ds.tokens, device="cpu").pin_memory()
-        self.h2d = sum(t.numel() * t.element_size() for d in self.h_in for t in d.values()) + \
-            self.h_logits.numel() * 4 + self.h_pos.numel() * 4 + self.h_seq.numel() * 4
+        self.h2d = sum(t.numel() * t.element_size() for _, t in srcs)
         self.d2h = self.h_tokens.numel() * 4
+        self.copy_stream = torch.cuda.Stream()
+        self._orig = ({l: {k: L[k] for k in self.KEYS} for l, L in enumerate(ds.layers)}, ds.logits, ds.pos, ds.seq,
+                      ds.tokens)
 
-    def run(self):
+    def _use(self, st):
+        ds, views = self.ds, st["views"]
+        for l, L in enumerate(ds.layers):
+            for k in self.KEYS:
+                L[k] = views[("layer", l, k)]
+        ds.logits, ds.pos, ds.seq, ds.tokens = views[("logits",)], views[("pos",)], views[("seq",)], st["tokens"]
+
+    def _restore(self):
         ds = self.ds
-        for L, H in zip(ds.layers, self.h_in):
-            for k, t in H.items():
-                L[k].copy_(t, non_blocking=True)
-        ds.logits.copy_(self.h_logits, non_blocking=True)
-        ds.pos.copy_(self.h_pos, non_blocking=True)
-        ds.seq.copy_(self.h_seq, non_blocking=True)
-        ds.run()
-        self.h_tokens.copy_(ds.tokens, non_blocking=True)
+        layers, ds.logits, ds.pos, ds.seq, ds.tokens = self._orig
+        for l, L in enumerate(ds.layers):
+            L.update(layers[l])
+
+    def run_steps(self, K: int):
+        """K steps: compute on the current stream, input copies on the copy stream, ordered by events."""
+        main, side = torch.cuda.current_stream(), self.copy_stream
+        side.wait_stream(main)
+        copied = [torch.cuda.Event() for _ in range(K)]
+        done = [torch.cuda.Event() for _ in range(K)]
+        with torch.cuda.stream(side):
+            for i in range(min(2, K)):
+                self.sets[i % 2]["flat"].copy_(self.h_flat, non_blocking=True)
+                copied[i].record(side)
+        for i in range(K):
+            main.wait_event(copied[i])
+            self._use(self.sets[i % 2])
+            self.ds.run()
+            done[i].record(main)
+            with torch.cuda.stream(side):
+                side.wait_event(done[i])              # step i has drawn its tokens and read its inputs
+                self.h_tokens.copy_(self.sets[i % 2]["tokens"], non_blocking=True)
+                if i + 2 < K:
+                    self.sets[i % 2]["flat"].copy_(self.h_flat, non_blocking=True)
+                    copied[i + 2].record(side)
+        main.wait_stream(side)
+        self._restore()
 
 
 # ---------------------------------------------------------------------------
@@ -548,27 +596,28 @@ def main():
 
     e2e = None
     if not args.no_e2e:
-        # End to end: every step copies its inputs in from pinned host memory and its tokens back out.
-        # In graph mode the copies are captured with the step (one graph replay per step).
+        # End to end: every step copies its inputs in from pinned host memory and its tokens back out,
+        # the next step's copies overlapping this step's kernels.  In graph mode the K steps, with their
+        # copies on a second stream, are one graph replayed once.
         hs = HostStep(ds)
-        hs.run()
+        hs.run_steps(2)
         torch.cuda.synchronize()
-        g_e2e = capture(hs.run) if graphs is not None else None
+        g_e2e = capture(lambda: hs.run_steps(K)) if graphs is not None else None
         barrier(dist)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record()
-        for _ in range(K):
-            if g_e2e is not None:
-                g_e2e.replay()
-            else:
-                hs.run()
+        if g_e2e is not None:
+            g_e2e.replay()
+        else:
+            hs.run_steps(K)
         e1.record()
         torch.cuda.synchronize()
         ems = max_over_ranks(dist, e0.elapsed_time(e1) / K, dev)
         e2e = {"value": sb["step"] * ws / (ems * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems,
                "h2d_bytes_per_step": hs.h2d, "d2h_bytes_per_step": hs.d2h,
-               "mode": "cuda_graph with copy nodes" if g_e2e is not None else "eager"}
+               "mode": ("cuda_graph with copy nodes" if g_e2e is not None else "eager") +
+                       ", one input copy per step, inputs and tokens double-buffered: copies overlap the previous step"}
 
     # the long-output workload: also the whole growing run, not only its last (longest) step
     long_output = time_long_output(ds, kv_bytes=1 if args.kv == "fp8" else 2) \
