@@ -265,18 +265,19 @@ class DeviceStep:
         self.run_sampler_only()
 
 
-def time_long_output(ds: DeviceStep, kv_bytes: int, chunk: int = 128) -> dict:
-    """The long-output run itself (batch 1): n_steps consecutive steps, step t appending key t of every layer,
-    attending t + 1 keys and sampling with the device step counter advancing.  Captured as graphs of `chunk`
-    steps (the lengths come from a device array, one element per step) and replayed back to back between two
-    events.  Overwrites the caches' first n_steps keys."""
+def time_long_output(ds: DeviceStep, kv_bytes: int, start: int = 0, chunk: int = 128) -> dict:
+    """The long-output run itself (batch 1): n_steps consecutive steps, step t appending key start + t of every
+    layer, attending start + t + 1 keys and sampling with the device step counter advancing.  Captured as
+    graphs of `chunk` steps (the lengths come from a device array, one element per step) and replayed back to
+    back between two events.  Overwrites the caches' keys start .. start + n_steps - 1."""
     w, api, dev = ds.w, ds.api, ds.dev
-    assert w.B == 1 and w.n_steps > 1
+    assert w.B == 1 and w.n_steps > 1 and start + w.n_steps <= w.cap
     T = w.n_steps
-    lens = torch.arange(1, T + 1, dtype=torch.int32, device=dev)
+    lens = torch.arange(start + 1, start + T + 1, dtype=torch.int32, device=dev)
     step = torch.zeros(1, dtype=torch.int32, device=dev)
 
     pos_all = lens - 1   # the separate append call reads its position from here
+    hint, ds.hint = ds.hint, start + T   # the run's own length bound
     graphs = []
     for t0 in range(0, T, chunk):
         g = torch.cuda.CUDAGraph()
@@ -290,6 +291,7 @@ def time_long_output(ds: DeviceStep, kv_bytes: int, chunk: int = 128) -> dict:
                                            V=w.V, advance=True)
         torch.cuda.current_stream().wait_stream(cs)
         graphs.append(g)
+    ds.hint = hint
     for g in graphs:                                          # untimed pass: first-touch costs
         g.replay()
     torch.cuda.synchronize()
@@ -301,9 +303,10 @@ def time_long_output(ds: DeviceStep, kv_bytes: int, chunk: int = 128) -> dict:
     e1.record()
     torch.cuda.synchronize()
     total_ms = e0.elapsed_time(e1)
-    total_bytes = sum(step_bytes(dataclasses.replace(w, seq_len=np.array([t + 1], np.int32)), kv_bytes=kv_bytes)["step"]
-                      for t in range(T))
-    return {"steps": T, "mean_us_per_step": total_ms * 1e3 / T, "GBps": total_bytes / (total_ms * 1e-3) / 1e9,
+    total_bytes = sum(step_bytes(dataclasses.replace(w, seq_len=np.array([start + t + 1], np.int32)),
+                                 kv_bytes=kv_bytes)["step"] for t in range(T))
+    return {"steps": T, "lengths": [start + 1, start + T], "mean_us_per_step": total_ms * 1e3 / T,
+            "GBps": total_bytes / (total_ms * 1e-3) / 1e9,
             "launches": T * ds.launches_per_step(),
             "timing": f"{len(graphs)} graphs of {chunk} steps replayed back to back, events around them"}
 
@@ -457,7 +460,21 @@ def time_oracle(w: W.Workload, steps: int, warmup: int = 0, min_seconds: float =
             f"all {w.H} heads) plus the sampler of every row and codebook, {n} repetition(s) in {dt:.1f} s, "
             f"jobs per (row, head) and per (row, codebook) on a thread pool of {cores}")
     return dict(value=gbs, unit="GB/s", cores=cores, kind="oracle", sample=desc,
-                seconds=dt, reps=n, bytes_per_step=sample.bytes)
+                seconds=dt, reps=n, bytes_per_step=sample.bytes, hardware_threads=os.cpu_count(),
+                one_thread_workload1=time_oracle_one_thread())
+
+
+def time_oracle_one_thread(min_seconds: float = 0.5) -> dict:
+    """The oracle on the smallest workload (one layer, batch 1, 64 + 64 keys, the sampler) on one thread."""
+    w1 = W.make_workload(1)
+    sample = OracleSample(w1, w1.B)
+    sample.run(1)
+    t0, n = time.perf_counter(), 0
+    while time.perf_counter() - t0 < min_seconds:
+        sample.run(1)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"us_per_step": dt / n * 1e6, "GBps": sample.bytes * n / dt / 1e9, "reps": n}
 
 
 # ---------------------------------------------------------------------------
@@ -498,7 +515,8 @@ def main():
         line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": ws,
                 "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
-                "cpu_baseline": {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "cpu_baseline": {k: r[k] for k in ("value", "unit", "cores", "kind", "sample", "hardware_threads",
+                                                   "one_thread_workload1")},
                 "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -619,14 +637,20 @@ def main():
                "mode": ("cuda_graph with copy nodes" if g_e2e is not None else "eager") +
                        ", one input copy per step, inputs and tokens double-buffered: copies overlap the previous step"}
 
-    # the long-output workload: also the whole growing run, not only its last (longest) step
-    long_output = time_long_output(ds, kv_bytes=1 if args.kv == "fp8" else 2) \
-        if w.n_steps > 1 and not args.eager else None
+    # the long-output workload: also the whole growing run, not only its last (longest) step, and the same
+    # number of steps growing from there to the cache's capacity
+    long_output = None
+    if w.n_steps > 1 and not args.eager:
+        kvb = 1 if args.kv == "fp8" else 2
+        long_output = time_long_output(ds, kv_bytes=kvb)
+        if 2 * w.n_steps <= w.cap:
+            long_output["continued"] = time_long_output(ds, kv_bytes=kvb, start=w.n_steps)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         r = time_oracle(w, 1, min_seconds=10.0)
-        cpu = {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu = {k: r[k] for k in ("value", "unit", "cores", "kind", "sample", "hardware_threads",
+                                 "one_thread_workload1")}
 
     assert int(ds.err.item()) == 0, "device error flag set during the timed steps"
     if rank == 0:
