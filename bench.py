@@ -26,6 +26,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -159,11 +160,15 @@ def measured_peaks():
 
 
 def sources_digest(names) -> str:
-    """First 16 hex digits of the SHA-256 of the named csrc files, concatenated in order."""
+    """First 16 hex digits of the SHA-256 of the named csrc files' code, concatenated in order.  Comments are
+    removed and whitespace collapsed first, so that only a change to the code itself voids a capture."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "decode_attention_self_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "decode_attention_self_gb300", "csrc", n)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                # line comments (no '//' inside strings here)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

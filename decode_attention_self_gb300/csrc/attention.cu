@@ -23,9 +23,17 @@
 //   (distributed shared memory), and rank 0 merges them after one cluster
 //   barrier.
 //
-// Roofline: a key costs 256 bytes (64 bf16 of K and of V) and ~260 flops, so
-// the kernel is bound by HBM bandwidth; there is no dense contraction for the
-// tensor cores (one query row).
+// Overlap with the previous kernel on the stream (programmatic dependent
+// launch): before waiting for it, each warp prefetches its tiles' K and V rows
+// into L2; a grid that is resident as a whole then lets the next kernel launch
+// at once, a larger one after its streaming.
+//
+// Self caches are bf16 or e4m3 (one byte per element with per-tensor k/v
+// scales, the KV-format trait below); the description encoder's K/V are bf16.
+//
+// Roofline: a key costs 256 bytes (64 bf16 of K and of V; 128 for e4m3) and
+// ~260 flops, so the kernel is bound by HBM bandwidth; there is no dense
+// contraction for the tensor cores (one query row).
 #include <cooperative_groups.h>
 #include <cuda_fp8.h>
 
@@ -313,15 +321,16 @@ __device__ __forceinline__ void attend_range(const AttnParams &p, bool cross_row
 }
 
 // L2 prefetch of the K and V rows of warp `warp`'s first kPrefetchTiles tiles
-// (the pipelined variant, whose whole grid is resident at once, prefetches its
-// whole range; the streaming variant its first two tiles), issued before the
-// kernel waits for its predecessor on the stream.  Only a hint: the
+// (the pipelined variant, whose whole grid is resident at once, takes up to 64,
+// its whole range for rows of up to 4096 keys per CTA; the streaming variant
+// its first two), issued before the kernel waits for its predecessor on the
+// stream.  Only a hint: the
 // length and the block table may still be changing (the predecessor may write
 // them), so they are read with relaxed loads, every address is checked against
 // the row's capacity or the block pool, and the real loads after the wait use
 // the final values.  L2 is coherent with the predecessor's writes.
 template <typename KV, bool kPaged, int kPrefetchTiles>
-__device__ __forceinline__ void prefetch_first_tiles(const AttnParams &p, bool cross, int b, int h, int split,
+__device__ __forceinline__ void prefetch_tiles(const AttnParams &p, bool cross, int b, int h, int split,
                                                      int nsplit, int warp) {
     constexpr uint32_t kRowBytes = (uint32_t)kD * KV::kElemBytes;
     const int cap = cross ? p.xcap : p.cap;
@@ -379,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
 
     // While the previous kernel on the stream drains, warm L2 with this warp's tiles; then wait for it.
     if (lane == 0) {
-        if (cross) prefetch_first_tiles<Bf16Kv, false, kPipelined ? 64 : 2>(p, true, b, h, split, nsplit, warp);
-        else prefetch_first_tiles<KV, kPaged, kPipelined ? 64 : 2>(p, false, b, h, split, nsplit, warp);
+        if (cross) prefetch_tiles<Bf16Kv, false, kPipelined ? 64 : 2>(p, true, b, h, split, nsplit, warp);
+        else prefetch_tiles<KV, kPaged, kPipelined ? 64 : 2>(p, false, b, h, split, nsplit, warp);
     }
     pdl_wait();
     // The next kernel on the stream may start launching: at once when this grid is resident as a whole
