@@ -24,7 +24,7 @@ DR_OK, DR_ERR_INVALID_ARG, DR_ERR_UNSUPPORTED, DR_ERR_CUDA = 0, 1, 2, 3
 DR_KV_CONTIGUOUS, DR_KV_PAGED = 0, 1
 DR_BF16, DR_F32 = 0, 1
 DR_KV_BF16, DR_KV_FP8_E4M3 = 0, 1
-DR_ERRF_SEQ_LEN, DR_ERRF_BLOCK_ID, DR_ERRF_POS, DR_ERRF_TOKEN = 1, 2, 4, 8
+DR_ERRF_SEQ_LEN, DR_ERRF_BLOCK_ID, DR_ERRF_POS, DR_ERRF_TOKEN, DR_ERRF_TIMEOUT = 1, 2, 4, 8, 16
 DR_SAMPLE_ADVANCE = 1
 
 if not os.path.exists(LIB_PATH):

@@ -6,12 +6,17 @@
  * Four operations make up one decode step:
  *   dr_kv_append            write this step's key/value into the cache;
  *   dr_decode_self_attn     one-query causal self-attention over the valid
- *                           length of a static (contiguous) or paged cache;
+ *                           length of a static (contiguous) or paged cache,
+ *                           bf16 or FP8 E4M3;
  *   dr_decode_cross_attn    one-query attention over the description
  *                           encoder's keys and values;
  *   dr_sample_topk_delayed  temperature, top-k, softmax and categorical draw
  *                           for every codebook in one kernel, under the
  *                           delay pattern.
+ * dr_decode_layer does the first three for one layer in one launch; the
+ * decoder's two ends around them are dr_lm_head (the merged codebook heads
+ * on the newest position, writing the logits the sampler reads) and
+ * dr_embed_tokens (the merged embedding lookup of the drawn tokens).
  *
  * Conventions shared by every call
  *   - Every pointer argument except `stream` is a DEVICE pointer owned by the
@@ -274,10 +279,11 @@ dr_status dr_embed_tokens(const int32_t *tokens, const void *table, int B, int C
  *   K      : 256, 512, 768, 1024, 1536 or 2048 (DR_ERR_UNSUPPORTED otherwise)
  *   err_flag : nullable device int32; DR_ERRF_TIMEOUT if a tensor-core CTA's
  *            bounded pipeline wait gave up (its logits are then not written)
- * fp32 accumulation.  Below 16 batch rows each logit is one CUDA-core dot
- * product in a fixed order; from 16 rows on the head is a dense contraction
+ * fp32 accumulation.  Below 4 batch rows each logit is one CUDA-core dot
+ * product in a fixed order; from 4 rows on the head is a dense contraction
  * on the tensor cores (tcgen05.mma, bf16 in, fp32 accumulate in tensor
- * memory, K consumed 16 at a time).
+ * memory, K consumed 16 at a time; for batch tiles of up to 32 rows the two
+ * halves of K are accumulated apart and added, the first half's sum first).
  */
 dr_status dr_lm_head(const void *hidden, const void *W, int B, int K, int C, int V, int ldv, float *logits,
                      int32_t *err_flag, void *stream);
