@@ -385,6 +385,9 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     if (b >= p.B) return;   // tail of the packed region (no cluster barrier is reached there)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // A split row's CTAs later write into CTA rank 0's shared memory; that needs every CTA of the cluster
+    // to have started.  Announce it now (no memory ordering), and wait for the others just before the write.
+    if (nsplit > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     // While the previous kernel on the stream drains, warm L2 with this warp's tiles; then wait for it.
     if (lane == 0) {
@@ -465,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     // visible to rank 0.  Nothing reads another CTA's shared memory after the barrier, so the other CTAs
     // may exit at once.
     cg::cluster_group cluster = cg::this_cluster();
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA of the cluster has started
     if (d < kD) {
         SoftmaxPartial *slot = cluster.map_shared_rank(&s_parts[split], 0);
         slot->acc[d] = o;
