@@ -229,3 +229,30 @@ def test_append_then_attend_sees_new_key():
     oracle.kv_append_contiguous(k, v, W.bits(kn), W.bits(vn), pos)
     after = oracle.attn_contiguous(W.bits(q), k, v, w.seq_len, SCALE)
     assert np.isfinite(after).all()
+
+
+def test_row_entry_points_equal_the_batch_ones():
+    # The per-row oracle calls (used for sampled checks at full size) must give, row by row, exactly what
+    # the pinned batch calls give.
+    rng = np.random.default_rng(31)
+    B, H, D, cap = 3, 2, 64, 40
+    lens = np.array([1, 17, 40], np.int32)
+    gen = torch.Generator().manual_seed(32)
+    q = W.bits(torch.randn((B, H, D), generator=gen).to(torch.bfloat16))
+    k = W.bits(torch.randn((B, H, cap, D), generator=gen).to(torch.bfloat16))
+    v = W.bits(torch.randn((B, H, cap, D), generator=gen).to(torch.bfloat16))
+    batch = oracle.attn_contiguous(q, k, v, lens, 0.125)
+    for b in range(B):
+        for h in range(H):
+            row = oracle.attn_contiguous_row(q[b, h], np.ascontiguousarray(k[b, h]), np.ascontiguousarray(v[b, h]),
+                                             int(lens[b]), 0.125)
+            assert np.array_equal(row, batch[b, h])
+    NB = 9
+    table = rng.permutation(NB)[:B * 3].reshape(B, 3).astype(np.int32)
+    kp = W.bits(torch.randn((NB, H, 16, D), generator=gen).to(torch.bfloat16))
+    vp = W.bits(torch.randn((NB, H, 16, D), generator=gen).to(torch.bfloat16))
+    pbatch = oracle.attn_paged(q, kp, vp, table, lens, 0.125)
+    for b in range(B):
+        for h in range(H):
+            row = oracle.attn_paged_row(q[b, h], kp, vp, table[b], h, int(lens[b]), 0.125)
+            assert np.array_equal(row, pbatch[b, h])

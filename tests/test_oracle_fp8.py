@@ -111,3 +111,31 @@ def test_fp8_paged_equals_contiguous():
     a = oracle.attn_fp8_contiguous(q, kc, vc, lens, 0.125, 0.1, 0.2)
     b_ = oracle.attn_fp8_paged(q, kp, vp, table, lens, 0.125, 0.1, 0.2)
     assert np.array_equal(a, b_)
+
+
+def test_fp8_paged_append_writes_the_contiguous_codes_at_the_logical_slot():
+    # The paged append must write, at block table[b][pos/16], slot pos % 16, the same codes the (pinned)
+    # contiguous append writes at position pos, and leave every other slot of the pool untouched.
+    rng = np.random.default_rng(7)
+    B, H, D, bs, NB = 3, 2, 64, 16, 7
+    kn = W.bits(torch.randn((B, H, D), generator=torch.Generator().manual_seed(8)).to(torch.bfloat16))
+    vn = W.bits(torch.randn((B, H, D), generator=torch.Generator().manual_seed(9)).to(torch.bfloat16))
+    pos = np.array([0, 17, 31], np.int32)
+    table = rng.permutation(NB)[:B * 2].reshape(B, 2).astype(np.int32)
+    kp = rng.integers(0, 0x7F, size=(NB, H, bs, D), dtype=np.uint8)
+    vp = rng.integers(0, 0x7F, size=(NB, H, bs, D), dtype=np.uint8)
+    kp0, vp0 = kp.copy(), vp.copy()
+    ks, vs = 0.05, 0.07
+    oracle.kv_append_fp8_paged(kp, vp, table, kn, vn, pos, ks, vs)
+    kc = np.zeros((B, H, 32, D), np.uint8)
+    vc = np.zeros((B, H, 32, D), np.uint8)
+    oracle.kv_append_fp8_contiguous(kc, vc, kn, vn, pos, ks, vs)
+    written = np.zeros((NB, bs), bool)
+    for b in range(B):
+        blk, slot = table[b, pos[b] // bs], pos[b] % bs
+        assert np.array_equal(kp[blk, :, slot], kc[b, :, pos[b]])
+        assert np.array_equal(vp[blk, :, slot], vc[b, :, pos[b]])
+        written[blk, slot] = True
+    untouched = ~written
+    assert np.array_equal(kp.transpose(0, 2, 1, 3)[untouched], kp0.transpose(0, 2, 1, 3)[untouched])
+    assert np.array_equal(vp.transpose(0, 2, 1, 3)[untouched], vp0.transpose(0, 2, 1, 3)[untouched])
