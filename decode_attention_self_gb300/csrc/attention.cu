@@ -74,8 +74,10 @@ struct Bf16Kv {
     __device__ static Chunk load(const uint8_t *p) { return ld_stream16(p); }
     __device__ static void store(uint8_t *p, const Chunk &c) { *reinterpret_cast<uint4 *>(p) = c; }
     __device__ static void unpack(const Chunk &c, float (&f)[kDims]) { unpack8(c, f); }
-    // This step's key/value (bf16 dims of this lane) in the cache's format.
-    __device__ static Chunk from_bf16(const uint16_t *src, float) { return ld_ro16(src); }
+    // This lane's chunk (dims sub*8 .. sub*8 + 7) of this step's key or value row src_row [D] bf16, in the
+    // cache's format.  kWarpNewRow: the whole warp must call new_row; else only the lanes that need it.
+    static constexpr bool kWarpNewRow = false;
+    __device__ static Chunk new_row(const uint16_t *src_row, float, int, int sub) { return ld_ro16(src_row + sub * 8); }
 };
 struct Fp8Kv {
     using Chunk = uint2;
@@ -86,8 +88,19 @@ struct Fp8Kv {
     __device__ static Chunk load(const uint8_t *p) { return ld_stream8(p); }
     __device__ static void store(uint8_t *p, const Chunk &c) { *reinterpret_cast<uint2 *>(p) = c; }
     __device__ static void unpack(const Chunk &c, float (&f)[kDims]) { unpack8_e4m3(c, f); }
-    // Quantise: code = e4m3(fl32(x / scale)), round to nearest even, saturating.
-    __device__ static Chunk from_bf16(const uint16_t *src, float scale) { return quantize8_e4m3(ld_ro16(src), scale); }
+    // The same for an e4m3 cache: code = e4m3(fl32(x / scale)), round to nearest even, saturating.  The IEEE
+    // divisions are spread over the warp -- lane L quantises dims 2L and 2L + 1 -- and each lane gathers its
+    // eight codes from lanes 4 sub .. 4 sub + 3 (a lane group alone would do 16 dependent divisions).
+    static constexpr bool kWarpNewRow = true;
+    __device__ static Chunk new_row(const uint16_t *src_row, float scale, int lane, int sub) {
+        const uint32_t two = __ldg(reinterpret_cast<const uint32_t *>(src_row) + lane);
+        const uint32_t codes = (uint32_t)__nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(bf16_lo(two), scale), __fdiv_rn(bf16_hi(two), scale)), __NV_SATFINITE, __NV_E4M3);
+        uint32_t c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[i] = __shfl_sync(0xFFFFFFFFu, codes, 4 * sub + i);
+        return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    }
 };
 
 // Merge (m2, l2, a2) into (m, l, a); an empty state has m = -inf, l = 0, a = 0.
@@ -220,14 +233,19 @@ __device__ __forceinline__ void attend_range(const AttnParams &p, bool cross_row
     auto load_tile = [&](int t, Chunk (&kw)[kKeys], Chunk (&vw)[kKeys]) -> bool {
         bool ok;
         const size_t base = tile_base(t, ok);
+        Chunk knew = KV::zero(), vnew = KV::zero();
+        if (KV::kWarpNewRow && kAppend && t <= newpos && newpos < t + kTile) {   // the same in the whole warp
+            knew = KV::new_row(p.k_new + row * kD, p.k_scale, lane, sub);
+            vnew = KV::new_row(p.v_new + row * kD, p.v_scale, lane, sub);
+        }
 #pragma unroll
         for (int u = 0; u < kKeys; ++u) {
             const int rr = grp + kGroups * u;
             const size_t off = base + (size_t)rr * kRowBytes + lane_off;
             if (ok && t + rr < key1) {
                 if (kAppend && t + rr == newpos) {
-                    kw[u] = KV::from_bf16(p.k_new + row * kD + sub * kDims, p.k_scale);
-                    vw[u] = KV::from_bf16(p.v_new + row * kD + sub * kDims, p.v_scale);
+                    kw[u] = KV::kWarpNewRow ? knew : KV::new_row(p.k_new + row * kD, p.k_scale, lane, sub);
+                    vw[u] = KV::kWarpNewRow ? vnew : KV::new_row(p.v_new + row * kD, p.v_scale, lane, sub);
                     KV::store(const_cast<uint8_t *>(kc) + off, kw[u]);
                     KV::store(const_cast<uint8_t *>(vc) + off, vw[u]);
                 } else {
