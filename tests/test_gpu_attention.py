@@ -134,6 +134,50 @@ def test_every_split_count(api, cuda_device, B):
     assert_attn_close(out, oracle_self(w, cache, q, default_scale(D)), f"B={B}, {S} CTAs per row")
 
 
+@pytest.mark.parametrize("mode", ["growing", "peaked", "zero_query", "huge"])
+def test_extreme_score_ranges(api, cuda_device, mode):
+    # growing: each key scores ~0.7 above the previous one in the log2 domain (~11 per 16-key tile, more than
+    #   the kernel's rescale slack of 8), so the running maximum moves and the state is rescaled tile after tile;
+    # peaked: one key of each row dominates the others by thousands;
+    # zero_query: every score is 0, so the output is the mean of the values;
+    # huge: scores in the thousands with both signs (most weights underflow to zero).
+    lens = [1, 40, 700, 3000]
+    w, cache, q = ragged_case("contiguous", lens, 3072, seed=61)
+    gen = torch.Generator().manual_seed(62)
+    u = torch.randn(D, generator=gen)
+    u = u / u.norm()
+    k = cache.k.float()
+    qf = q.float()
+    if mode == "growing":
+        c = torch.arange(3072, dtype=torch.float32) / 2.0            # q.k grows by 4 per key: 0.5 after x 1/8
+        k = 0.1 * k + c.view(1, 1, -1, 1) * u.view(1, 1, 1, -1)
+        qf = 8.0 * u.expand_as(qf).clone()
+    elif mode == "peaked":
+        k = 0.1 * k
+        for b, L in enumerate(lens):
+            k[b, :, (L - 1) // 2] = 300.0 * u
+        qf = 8.0 * u.expand_as(qf).clone()
+    elif mode == "zero_query":
+        qf = torch.zeros_like(qf)
+    else:
+        k = 40.0 * k
+        qf = 40.0 * qf
+    cache.k = k.to(torch.bfloat16)
+    q = qf.to(torch.bfloat16)
+    kv = to_dev(cache, cuda_device)
+    out = torch.empty((w.B, w.H, D), dtype=torch.float32, device=cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    api.dr_decode_self_attn(q.to(cuda_device), kv, torch.from_numpy(w.seq_len).to(cuda_device), out, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle_self(w, cache, q, default_scale(D))
+    if mode == "zero_query":   # the plain mean, independently of the oracle
+        vv = cache.v.double().numpy()
+        for b, L in enumerate(lens):
+            np.testing.assert_allclose(ref[b], vv[b, :, :L].mean(axis=1), rtol=0, atol=1e-12)
+    assert_attn_close(out, ref, f"scores {mode}")
+
+
 @pytest.mark.parametrize("L", [1, 17, 1000, 4095, 4096])
 def test_batch1_long_rows(api, cuda_device, L):
     w, cache, q = ragged_case("contiguous", [L], 4096, seed=3)
