@@ -32,20 +32,30 @@ __global__ void __launch_bounds__(kEmbThreads) embed_tokens_kernel(const EmbedPa
     pdl_trigger();
     const int b = blockIdx.x;
     const int chunks = p.Dm / 8;
+    // the row's tokens first (the same for every thread), so that all C row loads are in flight at once
+    int tok[kMaxCodebooks];
+    bool ok[kMaxCodebooks];
+#pragma unroll
+    for (int c = 0; c < kMaxCodebooks; ++c) {
+        tok[c] = c < p.C ? __ldg(p.tokens + (size_t)b * p.C + c) : 0;
+        ok[c] = c < p.C && (unsigned)tok[c] < (unsigned)p.V;
+        if (c < p.C && !ok[c] && threadIdx.x == 0) flag_error(p.err, DR_ERRF_TOKEN);
+    }
     for (int ch = threadIdx.x; ch < chunks; ch += kEmbThreads) {
+        uint4 e[kMaxCodebooks];
+#pragma unroll
+        for (int c = 0; c < kMaxCodebooks; ++c)
+            if (ok[c]) e[c] = ld_ro16(p.table + ((size_t)c * p.V + tok[c]) * p.Dm + ch * 8);
         float acc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-        for (int c = 0; c < p.C; ++c) {
-            const int tok = __ldg(p.tokens + (size_t)b * p.C + c);
-            if ((unsigned)tok >= (unsigned)p.V) {
-                if (ch == 0) flag_error(p.err, DR_ERRF_TOKEN);
-                continue;
-            }
-            float e[8];
-            unpack8(ld_ro16(p.table + ((size_t)c * p.V + tok) * p.Dm + ch * 8), e);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] += e[j];
+        for (int c = 0; c < kMaxCodebooks; ++c) {   // fp32 sum in codebook order
+            if (!ok[c]) continue;
+            float f[8];
+            unpack8(e[c], f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += f[j];
         }
         if (p.out_f32) {
             float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + (size_t)b * p.Dm + ch * 8);
