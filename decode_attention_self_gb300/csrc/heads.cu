@@ -73,96 +73,80 @@ __global__ void __launch_bounds__(kEmbThreads) embed_tokens_kernel(const EmbedPa
 }
 
 // ---------------------------------------------------------------------------
-// LM head: warp w of CTA g owns weight rows n = (g*kWarps + w)*kRows + r.
-// Lane l holds the 16-byte chunks l, l+32, ... of each of its rows (K/256 per
-// row) for the whole launch; hidden vectors are staged kBatch at a time in
-// shared memory and every row is dotted with each of them.
+// LM head below kLmHeadTensorCoreMinBatch rows: a persistent grid of one wave
+// (KC <= 4: four CTAs per SM).  Warp w of the grid takes weight rows w, w + W,
+// w + 2W, ... (W = warps in the grid); lane l holds the 16-byte chunks l,
+// l+32, ... of its current row while the next row's loads are in flight, and
+// dots it with every hidden vector (staged once in shared memory).  Each logit
+// is the same fp32 sum in the same order as a per-row kernel would make it.
 // ---------------------------------------------------------------------------
 constexpr int kHeadWarps = 8;
 constexpr int kHeadThreads = kHeadWarps * 32;
-constexpr int kRows = 2;      // weight rows per warp
-constexpr int kBatch = 16;    // hidden vectors per shared-memory stage
+static_assert(kLmHeadTensorCoreMinBatch <= 4, "the hidden vectors of the CUDA-core head fit shared memory");
 
 template <int KC>   // 16-byte chunks per lane per row: K = 256 * KC
-__global__ void __launch_bounds__(kHeadThreads) lm_head_kernel(const LmHeadParams p) {
-    extern __shared__ uint4 s_hidden[];   // [kBatch][K/8]
+constexpr int head_ctas_per_sm() { return KC <= 4 ? 4 : 2; }
+
+template <int KC>
+__global__ void __launch_bounds__(kHeadThreads, head_ctas_per_sm<KC>()) lm_head_kernel(const LmHeadParams p) {
+    extern __shared__ uint4 s_hidden[];   // [B][K/8]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = (blockIdx.x * kHeadWarps + warp) * kRows;
     const int N = p.C * p.V;
     const int kchunks = 32 * KC;
-    // The weights are parameters, not an output of the previous kernel: warm L2 with this warp's rows
-    // (contiguous) while that kernel drains, then wait for it.
-    if (lane == 0 && n0 < N)
-        prefetch_l2(p.W + (size_t)n0 * (kchunks * 8), (uint32_t)(min(kRows, N - n0) * kchunks * 16));
+    const size_t row_elems = (size_t)kchunks * 8;
+    const int gw = (int)gridDim.x * kHeadWarps;
+    const int n0 = (int)blockIdx.x * kHeadWarps + warp;
+    // The weights are parameters, not an output of the previous kernel: warm L2 with this warp's first two
+    // rows while that kernel drains, then wait for it.
+    if (lane == 0) {
+        if (n0 < N) prefetch_l2(p.W + (size_t)n0 * row_elems, (uint32_t)kchunks * 16u);
+        if (n0 + gw < N) prefetch_l2(p.W + (size_t)(n0 + gw) * row_elems, (uint32_t)kchunks * 16u);
+    }
     pdl_wait();
     pdl_trigger();
 
-    uint4 wr[kRows][KC];
+    uint4 cur[KC];
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-        const int n = n0 + r;
+    for (int j = 0; j < KC; ++j)
+        cur[j] = n0 < N ? ld_stream16(p.W + (size_t)n0 * row_elems + (size_t)(lane + 32 * j) * 8) : make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < p.B * kchunks; i += kHeadThreads) s_hidden[i] = ld_ro16(p.hidden + (size_t)i * 8);
+    __syncthreads();
+
+    for (int n = n0; n < N; n += gw) {
+        const int nn = n + gw;
+        uint4 nxt[KC];
 #pragma unroll
         for (int j = 0; j < KC; ++j)
-            wr[r][j] = n < N ? ld_stream16(p.W + (size_t)n * (kchunks * 8) + (size_t)(lane + 32 * j) * 8)
-                             : make_uint4(0, 0, 0, 0);
-    }
-
-    for (int b0 = 0; b0 < p.B; b0 += kBatch) {
-        const int nb = min(kBatch, p.B - b0);
-        __syncthreads();   // the previous stage is no longer read
-        for (int i = threadIdx.x; i < nb * kchunks; i += kHeadThreads) {
-            const int bb = i / kchunks, ch = i - bb * kchunks;
-            s_hidden[i] = ld_ro16(p.hidden + ((size_t)(b0 + bb) * kchunks + ch) * 8);
-        }
-        __syncthreads();
-        for (int bb = 0; bb < nb; ++bb) {
-            float acc[kRows];
-#pragma unroll
-            for (int r = 0; r < kRows; ++r) acc[r] = 0.f;
+            nxt[j] = nn < N ? ld_stream16(p.W + (size_t)nn * row_elems + (size_t)(lane + 32 * j) * 8)
+                            : make_uint4(0, 0, 0, 0);
+        const int c = n / p.V, vi = n - c * p.V;
+        for (int bb = 0; bb < p.B; ++bb) {
+            float acc = 0.f;
 #pragma unroll
             for (int j = 0; j < KC; ++j) {
-                float h[8];
+                float h[8], w[8];
                 unpack8(s_hidden[bb * kchunks + lane + 32 * j], h);
+                unpack8(cur[j], w);
 #pragma unroll
-                for (int r = 0; r < kRows; ++r) {
-                    float w[8];
-                    unpack8(wr[r][j], w);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[r] = fmaf(h[e], w[e], acc[r]);
-                }
+                for (int e = 0; e < 8; ++e) acc = fmaf(h[e], w[e], acc);
             }
 #pragma unroll
-            for (int r = 0; r < kRows; ++r) {
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xFFFFFFFFu, acc[r], o);
-            }
-            if (lane < kRows) {
-                const int n = n0 + lane;
-                float v = acc[0];
-#pragma unroll
-                for (int r = 1; r < kRows; ++r)
-                    if (lane == r) v = acc[r];
-                if (n < N) {
-                    const int c = n / p.V, vi = n - c * p.V;
-                    p.logits[((size_t)(b0 + bb) * p.C + c) * p.ldv + vi] = v;
-                }
-            }
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+            if (lane == 0) p.logits[((size_t)bb * p.C + c) * p.ldv + vi] = acc;
         }
+#pragma unroll
+        for (int j = 0; j < KC; ++j) cur[j] = nxt[j];
     }
 }
 
 template <int KC>
 cudaError_t launch_head(const LmHeadParams &p, cudaStream_t stream) {
     const int N = p.C * p.V;
-    const int rows_per_cta = kHeadWarps * kRows;
-    const unsigned grid = (unsigned)((N + rows_per_cta - 1) / rows_per_cta);
-    const size_t smem = (size_t)kBatch * 32 * KC * sizeof(uint4);
-    auto kern = lm_head_kernel<KC>;
-    if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    return launch_kernel(kern, dim3(grid), dim3(kHeadThreads), smem, stream, 1u, p);
+    const int by_rows = (N + kHeadWarps - 1) / kHeadWarps;
+    const int one_wave = head_ctas_per_sm<KC>() * current_device_sms();
+    const unsigned grid = (unsigned)(by_rows < one_wave ? by_rows : one_wave);
+    const size_t smem = (size_t)p.B * 32 * KC * sizeof(uint4);
+    return launch_kernel(lm_head_kernel<KC>, dim3(grid), dim3(kHeadThreads), smem, stream, 1u, p);
 }
 
 }  // namespace
