@@ -109,6 +109,16 @@ def test_few_distinct_values(api, cuda_device, k):
     check(api, cuda_device, logits, 1.0, k, np.arange(6, dtype=np.uint64) + 11, np.full(6, 20, np.int32), 1024)
 
 
+@pytest.mark.parametrize("k", [1, 7, 20, 40])
+def test_signed_zeros_tie_by_index(api, cuda_device, k):
+    # -0.0 and +0.0 are equal values: at the top-k boundary they tie and the lower index wins, whatever the
+    # sign bit (the kernel's order keys must not separate them).
+    rng = np.random.default_rng(70 + k)
+    vals = np.array([-0.0, 0.0, -0.0, 0.0, 1.0, -1.0, -np.inf], np.float32)
+    logits = vals[rng.choice(len(vals), size=(4, 9, 64), p=[0.3, 0.3, 0.15, 0.15, 0.04, 0.04, 0.02])]
+    check(api, cuda_device, logits, 1.0, k, np.arange(4, dtype=np.uint64) + 3, np.full(4, 20, np.int32), 63)
+
+
 def test_all_equal_logits_take_the_first_k(api, cuda_device):
     x = np.zeros((2, 9, 1088), np.float32)
     tok, pr, _ = run_gpu(api, cuda_device, x, 1.0, 50, np.array([1, 2], np.uint64), np.array([20, 20], np.int32), 5)
