@@ -149,7 +149,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag, cta_ok;
 
-    pdl_wait();
+    if (threadIdx.x == 0) {   // fetch the two tensor-map descriptors early
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_h)) : "memory");
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ks = p.ksplit;
     const int kpart = (int)blockIdx.x % ks;   // rank in the cluster
@@ -185,6 +188,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base;
+    // Everything above is set-up that reads nothing an earlier kernel writes, so it overlaps the previous
+    // kernel's tail; the hidden states and the logits' buffer are used only after this wait.
+    pdl_wait();
 
     if (warp == 0 && lane == 0) {
         // producer: stage s of round `round` (parity round & 1) waits for the MMAs of round - 1
