@@ -130,3 +130,40 @@ def test_split_plan(lib):
     assert plan(1, 16, 200, BF16, 152) == 4       # 13 tiles, at least 4 per CTA: ceil(13 / 4) = 4 CTAs
     assert plan(128, 16, 4096, 7, 152) == 1       # unknown storage type
     assert plan(0, 16, 4096, BF16, 152) == 1
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++11")])
+def test_header_compiles_alone_as_strict_c_and_cpp(lang, std):
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    flags = ["-Wall", "-Wextra", "-Werror"] + (["-pedantic"] if lang == "c" else [])
+    subprocess.run([cc, std, *flags, "-fsyntax-only", "-x", lang, HEADER], check=True)
+
+
+def test_plain_c_program_links_and_calls_the_library(lib, tmp_path):
+    # A C99 program that includes only dr_api.h, takes every entry point as a C function pointer and calls the
+    # two host-only ones: the ABI is usable from C without any C++ or CUDA header.
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no host compiler")
+    from decode_attention_self_gb300 import build
+
+    pkg = os.path.dirname(build.LIB)
+    src = tmp_path / "use_dr_api.c"
+    entry = ", ".join(f"(fn){n}" for n in declared_functions())
+    src.write_text('#include <stdio.h>\n#include "dr_api.h"\ntypedef void (*fn)(void);\n'
+                   f"int main(void) {{\n    fn all[] = {{{entry}}};\n"
+                   '    printf("%s %d %d\\n", dr_status_string(DR_OK), dr_plan_splits(128, 16, 4096, DR_KV_BF16, 152),\n'
+                   "           (int)(sizeof all / sizeof all[0]));\n    return 0;\n}\n")
+    exe = tmp_path / "use_dr_api"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.dirname(HEADER),
+                    str(src), "-L", pkg, "-ldecoderattn", f"-Wl,-rpath,{pkg}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    assert out == ["ok", "4", str(len(declared_functions()))]
