@@ -398,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     const bool packed = cross && p.xpacked;
     const int split = packed ? 0 : (int)blockIdx.x;
     const int nsplit = packed ? 1 : (int)gridDim.x;
-    const int b = !cross ? (int)blockIdx.z
-                         : packed ? ((int)blockIdx.z - p.B) * (int)gridDim.x + (int)blockIdx.x : (int)blockIdx.z - p.B;
+    int b = !cross ? (int)blockIdx.z
+                   : packed ? ((int)blockIdx.z - p.B) * (int)gridDim.x + (int)blockIdx.x : (int)blockIdx.z - p.B;
     if (b >= p.B) return;   // tail of the packed region (no cluster barrier is reached there)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -413,6 +413,10 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
         else prefetch_tiles<KV, kPaged, kPipelined ? 64 : 2>(p, false, b, h, split, nsplit, warp);
     }
     pdl_wait();
+    // The row index taken through a warp shuffle (the same value): measured, the compiler then schedules the
+    // row's address arithmetic so that the standalone bf16 kernel streams 4-13% faster (batch 32: 32.8 ->
+    // 28.3 us); the other variants time the same either way.
+    b = __shfl_sync(0xFFFFFFFFu, b, 0);
     // The next kernel on the stream may start launching: at once when this grid is resident as a whole
     // (its CTAs take free slots and prefetch), else once the streaming is done (below), so that they do
     // not take the slots of this grid's later waves.
