@@ -414,8 +414,8 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
     }
     pdl_wait();
     // The row index taken through a warp shuffle (the same value): measured, the compiler then schedules the
-    // row's address arithmetic so that the standalone bf16 kernel streams 4-13% faster (batch 32: 32.8 ->
-    // 28.3 us); the other variants time the same either way.
+    // row's address arithmetic so that the standalone bf16 kernel on a paged cache streams 4-13% faster
+    // (batch 32: 32.8 -> 28.3 us); the other variants time the same either way.
     b = __shfl_sync(0xFFFFFFFFu, b, 0);
     // The next kernel on the stream may start launching: at once when this grid is resident as a whole
     // (its CTAs take free slots and prefetch), else once the streaming is done (below), so that they do
