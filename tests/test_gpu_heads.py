@@ -78,7 +78,7 @@ def test_embed_invalid_token_is_left_out_and_flagged(api, cuda_device):
 @pytest.mark.parametrize("B,K", [
     (1, 1024), (3, 1024), (2, 256), (2, 512), (2, 2048),          # CUDA cores (batch < 4)
     (4, 1024), (15, 1024), (16, 1024), (17, 1024), (32, 2048),    # tensor cores, K split over a 2-CTA cluster
-    (33, 1024), (64, 256), (128, 1024),                           # tensor cores, one CTA per weight slab
+    (33, 1024), (64, 256), (80, 512), (100, 1024), (128, 1024),   # tensor cores, the batch cut in two tiles
     (200, 2048), (256, 768), (300, 1024), (513, 512)])            # tensor cores, several batch tiles
 def test_lm_head(api, cuda_device, B, K):
     dev = cuda_device
