@@ -282,8 +282,9 @@ dr_status dr_embed_tokens(const int32_t *tokens, const void *table, int B, int C
  * fp32 accumulation.  Below 4 batch rows each logit is one CUDA-core dot
  * product in a fixed order; from 4 rows on the head is a dense contraction
  * on the tensor cores (tcgen05.mma, bf16 in, fp32 accumulate in tensor
- * memory, K consumed 16 at a time; for batch tiles of up to 32 rows the two
- * halves of K are accumulated apart and added, the first half's sum first).
+ * memory, K consumed 16 at a time; when the batch is one tile of up to 32
+ * rows and the 128-row weight slabs are fewer than the SMs, the two halves of
+ * K are accumulated apart and added, the first half's sum first).
  */
 dr_status dr_lm_head(const void *hidden, const void *W, int B, int K, int C, int V, int ldv, float *logits,
                      int32_t *err_flag, void *stream);
