@@ -188,6 +188,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base;
+    // The weight boxes of the first ring round go into L2 now, a hint issued before the wait (the weights may
+    // in principle be an earlier kernel's output, so the loads themselves come after it): batch 4-32 about
+    // 0.3 us faster; prefetching the whole slab this way was slower at most batches.
+    if (warp == 0 && lane == 0) {
+        const int npf = chunks < p.stages ? chunks : p.stages;
+        for (int kc = 0; kc < npf; ++kc)
+            asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                             reinterpret_cast<uint64_t>(&map_w)),
+                         "r"((kc0 + kc) * kChunkK), "r"(n0)
+                         : "memory");
+    }
     // Everything above is set-up that reads nothing an earlier kernel writes, so it overlaps the previous
     // kernel's tail; the hidden states and the logits' buffer are used only after this wait.
     pdl_wait();
