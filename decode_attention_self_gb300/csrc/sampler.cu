@@ -42,8 +42,12 @@ namespace cg = cooperative_groups;
 namespace dr {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+// Threads per CTA: 256 while the grid fits the GPU at once with four such CTAs per SM (the register bound);
+// 128 for larger grids, so that twice the CTAs are resident and the grid still runs as one wave (batch 128:
+// 1152 CTAs, in clusters of 9 with DR_SAMPLE_ADVANCE).
+constexpr int kWideThreads = 256;
+constexpr int kNarrowThreads = 128;
+constexpr int kWideCtasPerSm = 4;
 
 // Philox4x32-10, Salmon, Moraes, Dror and Shaw, SC'11, section 3.
 __device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1) {
@@ -75,6 +79,7 @@ __device__ __forceinline__ bool better(float s, int i, float bs, int bi) {
 }
 
 // Block-wide exclusive prefix sum of one value per thread (all threads call).
+template <int kWarps>
 __device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int inc = v;
@@ -97,10 +102,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int &tot
     return before + inc - v;
 }
 
-template <int EPT>
-__global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) {
+template <int EPT, int kThreads>
+__global__ void __launch_bounds__(kThreads, kThreads == kNarrowThreads ? 8 : kWideCtasPerSm) sample_kernel(const SampleParams p) {
+    constexpr int kWarps = kThreads / 32;
     __shared__ uint32_t s_hist[2][256];
-    __shared__ uint32_t s_wtot[kWarps];
     __shared__ int s_sel[3];   // selected digit, keys still needed, keys in the digit's bin
     __shared__ uint32_t s_bal[EPT][kWarps];
     __shared__ int s_scan[kWarps];
@@ -135,8 +140,10 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) 
                 valid |= 1u << j;
             }
         }
-        s_hist[0][t] = 0u;
-        s_hist[1][t] = 0u;
+        for (int i = t; i < 256; i += kThreads) {
+            s_hist[0][i] = 0u;
+            s_hist[1][i] = 0u;
+        }
         __syncthreads();
 
         // ---- radix select of the top_k-th largest key ------------------------
@@ -152,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) 
                 if (((valid >> j) & 1u) && (key[j] & pmask) == prefix) atomicAdd(&hist[(key[j] >> shift) & 255u], 1u);
             }
             __syncthreads();
-            s_hist[(pass + 1) & 1][t] = 0u;   // the other buffer is free: clear it for the next pass
+            for (int i = t; i < 256; i += kThreads) s_hist[(pass + 1) & 1][i] = 0u;   // free now: clear it for the next pass
             if (warp == 0) {
                 // lane l scans digits 255 - 8l down to 248 - 8l; a warp scan orders the lanes
                 uint32_t c8[8], sum = 0u;
@@ -231,7 +238,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) 
         }
         // compact the kept indices (top_k of them) into s_list
         int total = 0;
-        int slot = block_exclusive_scan(nmine, s_scan, total);
+        int slot = block_exclusive_scan<kWarps>(nmine, s_scan, total);
 #pragma unroll
         for (int j = 0; j < EPT; ++j)
             if ((member >> j) & 1u) s_list[slot++] = t + kThreads * j;
@@ -331,10 +338,10 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleParams p) 
     }
 }
 
-template <int EPT>
+template <int EPT, int kThreads>
 cudaError_t launch_ept(const SampleParams &p, cudaStream_t stream) {
     const bool clustered = (p.flags & DR_SAMPLE_ADVANCE) && p.C > 1;
-    auto kern = sample_kernel<EPT>;
+    auto kern = sample_kernel<EPT, kThreads>;
     if (clustered && p.C > 8) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
@@ -346,12 +353,20 @@ cudaError_t launch_ept(const SampleParams &p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_sample(const SampleParams &p, cudaStream_t stream) {
-    const int ept = (p.V + kThreads - 1) / kThreads;
-    if (ept <= 1) return launch_ept<1>(p, stream);
-    if (ept <= 2) return launch_ept<2>(p, stream);
-    if (ept <= 4) return launch_ept<4>(p, stream);
-    if (ept <= 5) return launch_ept<5>(p, stream);
-    return launch_ept<8>(p, stream);
+    const long long ctas = (long long)p.B * p.C;
+    if (ctas <= (long long)kWideCtasPerSm * current_device_sms()) {
+        const int ept = (p.V + kWideThreads - 1) / kWideThreads;
+        if (ept <= 1) return launch_ept<1, kWideThreads>(p, stream);
+        if (ept <= 2) return launch_ept<2, kWideThreads>(p, stream);
+        if (ept <= 4) return launch_ept<4, kWideThreads>(p, stream);
+        if (ept <= 5) return launch_ept<5, kWideThreads>(p, stream);
+        return launch_ept<8, kWideThreads>(p, stream);
+    }
+    const int ept = (p.V + kNarrowThreads - 1) / kNarrowThreads;
+    if (ept <= 2) return launch_ept<2, kNarrowThreads>(p, stream);
+    if (ept <= 4) return launch_ept<4, kNarrowThreads>(p, stream);
+    if (ept <= 9) return launch_ept<9, kNarrowThreads>(p, stream);
+    return launch_ept<16, kNarrowThreads>(p, stream);
 }
 
 }  // namespace dr

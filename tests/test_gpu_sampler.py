@@ -178,6 +178,40 @@ def test_advance_flag_increments_step_once_per_call(api, cuda_device):
         assert np.array_equal(st.cpu().numpy(), steps0 + it + 1)
 
 
+@pytest.mark.parametrize("V", [5, 257, 1088, 2048])
+def test_large_grid(api, cuda_device, V):
+    # 128 rows x 9 codebooks: more CTAs than the GPU holds at once at 256 threads, so the sampler runs
+    # 128-thread CTAs (each thread keeps twice the keys).  Half the rows draw from few distinct values, so
+    # the top-k boundary ties and the radix select ends at different passes.
+    rng = np.random.default_rng(300 + V)
+    B = 128
+    x = (rng.normal(size=(B, 9, V)) * 3).astype(np.float32)
+    vals = np.array([-2.0, -0.5, 0.0, 0.5, 1.0, 1.0078125, 3.0], np.float32)
+    x[::2] = vals[rng.integers(0, len(vals), size=(B // 2, 9, V))]
+    steps = rng.integers(0, 12, size=B).astype(np.int32)
+    for k in sorted({1, min(V, 50), min(V, 250), V}):
+        check(api, cuda_device, x, 0.8, k, np.arange(B, dtype=np.uint64) + 5, steps, V - 1)
+
+
+def test_advance_flag_large_grid(api, cuda_device):
+    rng = np.random.default_rng(7)
+    B = 128
+    x = (rng.normal(size=(B, 9, 1088)) * 3).astype(np.float32)
+    steps0 = rng.integers(0, 20, size=B).astype(np.int32)
+    seeds = np.arange(B, dtype=np.uint64) + 1
+    dev = cuda_device
+    lg = torch.from_numpy(x).to(dev)
+    sd = torch.from_numpy(seeds.view(np.int64)).to(dev)
+    st = torch.from_numpy(steps0.copy()).to(dev)
+    tok = torch.empty((B, 9), dtype=torch.int32, device=dev)
+    for it in range(2):
+        api.dr_sample_topk_delayed(lg, 1.0, 50, sd, st, 1024, tok, advance=True)
+        torch.cuda.synchronize()
+        ref = oracle.sample(x, 1.0, 50, seeds, steps0 + it, 1024)
+        assert_tokens_match(tok, ref)
+        assert np.array_equal(st.cpu().numpy(), steps0 + it + 1)
+
+
 def test_deterministic(api, cuda_device):
     w = W.make_workload(5)
     x = W.make_logits(w).numpy()
