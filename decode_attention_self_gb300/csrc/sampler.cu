@@ -7,8 +7,9 @@
 // sampling without a GPU-CPU synchronisation; the architecture overview --
 // nine DAC codebooks, one token each per step, in a delayed pattern.
 //
-// Grid (C, B): one CTA of 256 threads per (codebook c, row b).  A CTA
-//   1. reads its V logits once (element i = t + 256 j stays in thread t's
+// Grid (C, B): one CTA of NT threads per (codebook c, row b), NT = 256, or 128
+// when the grid would not fit the GPU at once with 256.  A CTA
+//   1. reads its V logits once (element i = t + NT j stays in thread t's
 //      registers), divides by T with IEEE round-to-nearest and maps each float
 //      to an order-preserving uint32 key;
 //   2. finds the top_k-th largest key tau by an 8-bit radix select of up to 4
