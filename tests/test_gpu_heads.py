@@ -97,6 +97,23 @@ def test_lm_head(api, cuda_device, B, K):
     assert (np.abs(got[:, :, :V] - ref) <= (K - 1) * 2 * U * mag + 1e-30).all()
 
 
+def test_lm_head_more_slabs_than_sms(api, cuda_device):
+    # 16 codebooks of 2048: 256 weight slabs of 128 rows, more than the SMs, so a batch of 64 stays one tile
+    # (no batch split) and the grid runs at two CTAs per SM.
+    dev = cuda_device
+    B, K, C, V = 64, 512, 16, 2048
+    hidden = W.randn_bf16((B, K), "cpu", 204, B, K)
+    Wt = (torch.randn((C * V, K), generator=torch.Generator().manual_seed(9)) * (3.0 / K ** 0.5)).to(torch.bfloat16)
+    logits = torch.full((B, C, V), float("nan"), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    api.dr_lm_head(hidden.to(dev), Wt.to(dev), C, logits, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.lm_head(W.bits(hidden), W.bits(Wt)).reshape(B, C, V)
+    mag = (np.abs(vals(W.bits(hidden))) @ np.abs(vals(W.bits(Wt))).T).reshape(B, C, V)
+    assert (np.abs(logits.cpu().numpy() - ref) <= (K - 1) * 2 * U * mag + 1e-30).all()
+
+
 def test_lm_head_feeding_the_sampler(api, cuda_device):
     dev = cuda_device
     B, K, C, V, T, k = 4, 1024, 9, 1088, 0.9, 50
