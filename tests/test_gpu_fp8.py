@@ -80,6 +80,26 @@ def test_fp8_self_attention(api, cuda_device, layout, hint, out_dtype):
     assert_attn_close(out, oracle_fp8(w, c, q), f"fp8 {layout} hint {hint}")
 
 
+# ceil(6 * 152 / (16 B)) CTAs per row (at most 8); an e4m3 row of 1024 keys is 128 KiB, under one CTA's share.
+FP8_SPLIT_BATCHES = {8: 8, 9: 7, 10: 6, 12: 5, 15: 4, 20: 3, 29: 2, 57: 1}
+
+
+@pytest.mark.parametrize("B", sorted(FP8_SPLIT_BATCHES))
+def test_fp8_every_split_count(api, cuda_device, B):
+    S = FP8_SPLIT_BATCHES[B]
+    assert api.dr_plan_splits(B, 16, 1024, api.DR_KV_FP8_E4M3, 152) == S
+    dev = cuda_device
+    rng = np.random.default_rng(400 + B)
+    # ragged rows, with short rows that leave some CTAs of their cluster without a tile
+    lens = [1024, 1, 16, 17] + [int(x) for x in rng.integers(1, 1024, size=B - 4, endpoint=True)]
+    w, c = ragged("paged", lens, 1024, 40 + B, filled=np.array(lens, np.int32))
+    q = W.randn_bf16((w.B, 16, D), "cpu", 303, B)
+    out = torch.empty((w.B, 16, D), dtype=torch.float32, device=dev)
+    api.dr_decode_self_attn(q.to(dev), dev_cache(api, c, dev), torch.from_numpy(w.seq_len).to(dev), out,
+                            max_seq_len_hint=1024)
+    assert_attn_close(out, oracle_fp8(w, c, q), f"fp8 B={B}, {S} CTAs per row")
+
+
 @pytest.mark.parametrize("index", [2, 4, 5])
 def test_fp8_fused_layer_workloads(api, cuda_device, index):
     dev = cuda_device
