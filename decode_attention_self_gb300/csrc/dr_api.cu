@@ -34,7 +34,7 @@ namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Validates a cache description for B rows of H heads; returns the row capacity (keys) or -1.
+// Validates a cache description; on success stores the keys a row can hold in *cap.
 dr_status check_cache(const dr_kv_cache *c, int *cap) {
     if (!c || !c->k || !c->v) return DR_ERR_INVALID_ARG;
     if (!aligned16(c->k) || !aligned16(c->v)) return DR_ERR_INVALID_ARG;
