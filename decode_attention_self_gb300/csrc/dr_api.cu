@@ -248,8 +248,9 @@ dr_status dr_sample_topk_delayed(const float *logits, int B, int C, int V, int l
                                  const uint64_t *seeds, int32_t *step, int32_t pad_id, int32_t *tokens, float *probs,
                                  int flags, void *stream) {
     if (!logits || !seeds || !step || !tokens) return DR_ERR_INVALID_ARG;
-    if (B < 1 || B > 0x7FFFFFFF || C < 1 || V < 1 || ldv < V) return DR_ERR_INVALID_ARG;
-    if (C > dr::kMaxCodebooks || V > dr::kMaxVocab) return DR_ERR_UNSUPPORTED;
+    if (B < 1 || C < 1 || V < 1 || ldv < V) return DR_ERR_INVALID_ARG;
+    // one CTA row per batch row: the grid's y dimension holds at most 65535
+    if (B > 65535 || C > dr::kMaxCodebooks || V > dr::kMaxVocab) return DR_ERR_UNSUPPORTED;
     if (top_k < 1 || top_k > V) return DR_ERR_INVALID_ARG;
     if (!(temperature > 0.f) || isinf(temperature)) return DR_ERR_INVALID_ARG;
     if (flags & ~DR_SAMPLE_ADVANCE) return DR_ERR_INVALID_ARG;

@@ -236,6 +236,7 @@ dr_status dr_decode_layer(const void *q, const dr_kv_cache *cache, const void *k
  *
  *   logits   : [B][C][ldv] float32 (device); columns [V, ldv) are never read.
  *              NaN logits give an undefined (but in-range or pad) token.
+ *   B        : batch rows, 1..65535 (DR_ERR_UNSUPPORTED above)
  *   C        : codebooks, 1..16          V : vocabulary, 1..2048, V <= ldv
  *   temperature : > 0 and finite          top_k : 1..V
  *   seeds    : [B] uint64 (device)

@@ -112,6 +112,8 @@ def test_sampler_validation(lib):
     assert lib.dr_sample_topk_delayed(*args(C=17)) == 2
     assert lib.dr_sample_topk_delayed(*args(V=4096, ldv=4096, k=5)) == 2
     assert lib.dr_sample_topk_delayed(*args(flags=2)) == 1
+    assert lib.dr_sample_topk_delayed(*args(B=0)) == 1
+    assert lib.dr_sample_topk_delayed(*args(B=65536)) == 2      # the grid holds one batch row per y index
     assert lib.dr_sample_topk_delayed(vp(FAKE), 1, 9, 1088, 1088, f(1.0), 50, None, vp(FAKE), 1024, vp(FAKE), None, 0,
                                       None) == 1
 
