@@ -158,7 +158,10 @@ dr_status dr_kv_append(const dr_kv_cache *cache, const void *k_new, const void *
  *              flagged DR_ERRF_SEQ_LEN (a row of length 0 outputs zeros)
  *   max_seq_len_hint : an upper bound the caller knows for max_b seq_len[b]
  *              (<= 0: the capacity).  It only tunes how each row's keys are
- *              split across CTAs; any value gives the same result.
+ *              split across CTAs (dr_plan_splits); any value gives a result
+ *              within the stated accuracy, and the same hint on the same
+ *              device gives the same bits (a different split changes only
+ *              the order of the fp32 sums).
  *   scale    : softmax scale; <= 0 selects 1/sqrt(D)
  *   out      : [B][H][D] in out_dtype (DR_BF16: round to nearest even)
  *   err_flag : nullable device int32 (DR_ERRF_SEQ_LEN, DR_ERRF_BLOCK_ID)
