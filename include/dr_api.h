@@ -54,7 +54,8 @@ extern "C" {
 typedef enum dr_status {
     DR_OK = 0,
     DR_ERR_INVALID_ARG = 1, /* null pointer, size out of range, misaligned pointer */
-    DR_ERR_UNSUPPORTED = 2, /* a valid but unimplemented shape (D != 64, block_size != 16, C > 16, V > 2048) */
+    DR_ERR_UNSUPPORTED = 2, /* a valid but unimplemented shape (D != 64, block_size != 16, C > 16, V > 2048,
+                               more than 65535 sampler rows) */
     DR_ERR_CUDA = 3         /* the CUDA runtime refused the launch */
 } dr_status;
 
