@@ -240,6 +240,9 @@ dr_status dr_decode_layer(const void *q, const dr_kv_cache *cache, const void *k
  *
  *   logits   : [B][C][ldv] float32 (device); columns [V, ldv) are never read.
  *              NaN logits give an undefined (but in-range or pad) token.
+ *              Where some x_i are +inf (an infinite logit, or a temperature
+ *              so small that logit / temperature overflows), the token is the
+ *              lowest such index and the probabilities are undefined.
  *   B        : batch rows, 1..65535 (DR_ERR_UNSUPPORTED above)
  *   C        : codebooks, 1..16          V : vocabulary, 1..2048, V <= ldv
  *   temperature : > 0 and finite          top_k : 1..V

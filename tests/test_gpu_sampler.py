@@ -218,3 +218,54 @@ def test_deterministic(api, cuda_device):
     a, pa, _ = run_gpu(api, cuda_device, x, w.temperature, w.top_k, w.seeds, w.steps, w.pad_id)
     b, pb, _ = run_gpu(api, cuda_device, x, w.temperature, w.top_k, w.seeds, w.steps, w.pad_id)
     assert torch.equal(a, b) and torch.equal(pa, pb)
+
+
+@pytest.mark.parametrize("C", [1, 2, 16])
+def test_advance_flag_every_cluster_shape(api, cuda_device, C):
+    # DR_SAMPLE_ADVANCE makes each row's C codebook CTAs one cluster: none for C = 1, two CTAs, and a
+    # non-portable cluster of 16
+    rng = np.random.default_rng(40 + C)
+    B = 6
+    x = (rng.normal(size=(B, C, 700)) * 3).astype(np.float32)
+    steps0 = np.array([0, 1, C - 1, C, C + 5, 1000], np.int32)
+    seeds = np.arange(B, dtype=np.uint64) * np.uint64(977) + np.uint64(3)
+    dev = cuda_device
+    lg = torch.from_numpy(x).to(dev)
+    sd = torch.from_numpy(seeds.view(np.int64)).to(dev)
+    st = torch.from_numpy(steps0.copy()).to(dev)
+    tok = torch.empty((B, C), dtype=torch.int32, device=dev)
+    for it in range(3):
+        api.dr_sample_topk_delayed(lg, 1.1, 30, sd, st, 700, tok, advance=True)
+        torch.cuda.synchronize()
+        ref = oracle.sample(x, 1.1, 30, seeds, steps0 + it, 700)
+        assert_tokens_match(tok, ref, f"C={C} call {it}")
+        assert np.array_equal(st.cpu().numpy(), steps0 + it + 1)
+
+
+def test_positive_infinity_and_a_tiny_temperature(api, cuda_device):
+    # x = logit / T at +inf (an infinite logit, or T so small that the division overflows): the +inf entries
+    # lead the top-k set (ties to the lower index) and each perturbed score x - log(-log u) of them is +inf,
+    # so the token is the lowest-index +inf entry; the probabilities are undefined there and not compared.
+    dev = cuda_device
+    rng = np.random.default_rng(50)
+    B, C, V = 4, 9, 300
+    x = (rng.normal(size=(B, C, V)) * 3).astype(np.float32)
+    for b in range(B):
+        for c in range(C):
+            x[b, c, rng.choice(V, size=1 + (b + c) % 4, replace=False)] = np.inf
+    seeds, steps = np.arange(B, dtype=np.uint64), np.full(B, 20, np.int32)
+    first_inf = np.argmax(np.isinf(x) & (x > 0), axis=2)
+    for k in (1, 2, 50, V):
+        tok, _, _ = run_gpu(api, dev, x, 1.0, k, seeds, steps, 1024, want_probs=False)
+        ref = oracle.sample(x, 1.0, k, seeds, steps, 1024)
+        assert np.array_equal(tok.cpu().numpy(), first_inf) and np.array_equal(ref["tokens"], first_inf), k
+    # a subnormal temperature: y / T overflows to +-inf for every |y| above 3.4e38 * T (binary32 division)
+    T = np.float32(1e-44)
+    y = rng.normal(size=(B, C, V)).astype(np.float32)
+    with np.errstate(over="ignore"):
+        xs = y / T
+    assert (np.isinf(xs) & (xs > 0)).any(axis=2).all()
+    first = np.argmax(np.isinf(xs) & (xs > 0), axis=2)
+    tok, _, _ = run_gpu(api, dev, y, float(T), 50, seeds, steps, 1024, want_probs=False)
+    ref = oracle.sample(y, float(T), 50, seeds, steps, 1024)
+    assert np.array_equal(tok.cpu().numpy(), first) and np.array_equal(ref["tokens"], first)
