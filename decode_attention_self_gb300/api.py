@@ -48,12 +48,13 @@ _lib.dr_decode_layer.argtypes = [_vp, ctypes.POINTER(dr_kv_cache), _vp, _vp, _vp
 _lib.dr_sample_topk_delayed.argtypes = [_vp, _i, _i, _i, _i, _f, _i, _vp, _vp, ctypes.c_int32, _vp, _vp, _i, _vp]
 _lib.dr_embed_tokens.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _i, _vp, _vp]
 _lib.dr_lm_head.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp]
+_lib.dr_lm_head_stall_test.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _i, _vp]
 _lib.dr_plan_splits.argtypes = [_i, _i, _i, _i, _i]
 _lib.dr_plan_splits.restype = _i
 _lib.dr_status_string.argtypes = [_i]
 _lib.dr_status_string.restype = ctypes.c_char_p
 for _fn in ("dr_kv_append", "dr_decode_self_attn", "dr_decode_cross_attn", "dr_decode_layer",
-            "dr_sample_topk_delayed", "dr_embed_tokens", "dr_lm_head"):
+            "dr_sample_topk_delayed", "dr_embed_tokens", "dr_lm_head", "dr_lm_head_stall_test"):
     getattr(_lib, _fn).restype = _i
 
 
@@ -237,6 +238,19 @@ def dr_lm_head(hidden: torch.Tensor, W: torch.Tensor, C: int, logits: torch.Tens
            _lib.dr_lm_head(_ptr(hidden, torch.bfloat16, "hidden"), _ptr(W, torch.bfloat16, "W"), B, K, C, V, ldv,
                            _ptr(logits, torch.float32, "logits"), _ptr(err_flag, torch.int32, "err_flag"),
                            _stream(stream)))
+    return logits
+
+
+def dr_lm_head_stall_test(hidden: torch.Tensor, W: torch.Tensor, C: int, logits: torch.Tensor, stall_slab: int,
+                          err_flag: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Test hook: dr_lm_head with the CTAs of weight slab `stall_slab` made to time out (see dr_api.h)."""
+    B, K = hidden.shape
+    V = W.shape[0] // C
+    ldv = logits.shape[2]
+    _check("dr_lm_head_stall_test",
+           _lib.dr_lm_head_stall_test(_ptr(hidden, torch.bfloat16, "hidden"), _ptr(W, torch.bfloat16, "W"), B, K, C, V,
+                                      ldv, _ptr(logits, torch.float32, "logits"),
+                                      _ptr(err_flag, torch.int32, "err_flag"), int(stall_slab), _stream(stream)))
     return logits
 
 

@@ -289,8 +289,13 @@ dr_status dr_embed_tokens(const int32_t *tokens, const void *table, int B, int C
     return from_cuda(dr::launch_embed_tokens(p, static_cast<cudaStream_t>(stream)));
 }
 
-dr_status dr_lm_head(const void *hidden, const void *W, int B, int K, int C, int V, int ldv, float *logits,
-                     int32_t *err_flag, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// dr_lm_head's checks and launch; stall_slab >= 0 only from the test hook below.
+dr_status lm_head_call(const void *hidden, const void *W, int B, int K, int C, int V, int ldv, float *logits,
+                       int32_t *err_flag, int stall_slab, void *stream) {
     if (!hidden || !W || !logits || !aligned16(hidden) || !aligned16(W)) return DR_ERR_INVALID_ARG;
     if (B < 1 || C < 1 || V < 1 || ldv < V || K < 1) return DR_ERR_INVALID_ARG;
     if ((long long)C * V > 0x7FFFFFFFLL) return DR_ERR_INVALID_ARG;
@@ -306,7 +311,25 @@ dr_status dr_lm_head(const void *hidden, const void *W, int B, int K, int C, int
     p.V = V;
     p.ldv = ldv;
     p.err = err_flag;
+    p.stall_slab = stall_slab;
     return from_cuda(dr::launch_lm_head(p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+dr_status dr_lm_head(const void *hidden, const void *W, int B, int K, int C, int V, int ldv, float *logits,
+                     int32_t *err_flag, void *stream) {
+    return lm_head_call(hidden, W, B, K, C, V, ldv, logits, err_flag, -1, stream);
+}
+
+dr_status dr_lm_head_stall_test(const void *hidden, const void *W, int B, int K, int C, int V, int ldv, float *logits,
+                                int32_t *err_flag, int stall_slab, void *stream) {
+    // only the tensor-core head has pipeline waits; the slab must exist
+    if (B < dr::kLmHeadTensorCoreMinBatch) return DR_ERR_UNSUPPORTED;
+    if (C < 1 || V < 1 || stall_slab < 0 || (long long)stall_slab * 128 >= (long long)C * V) return DR_ERR_INVALID_ARG;
+    return lm_head_call(hidden, W, B, K, C, V, ldv, logits, err_flag, stall_slab, stream);
 }
 
 const char *dr_status_string(dr_status s) {

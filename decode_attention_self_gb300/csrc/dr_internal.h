@@ -127,6 +127,9 @@ struct LmHeadParams {
     float *logits;           // [B][C][ldv]
     int32_t B, K, C, V, ldv;
     int32_t *err;
+    // Test hook (tensor-core head only): the CTAs of this 128-row weight slab never load their first K chunk,
+    // so their bounded pipeline wait runs out; -1 (every ordinary call): none.
+    int32_t stall_slab = -1;
 };
 
 cudaError_t launch_lm_head(const LmHeadParams &p, cudaStream_t stream);

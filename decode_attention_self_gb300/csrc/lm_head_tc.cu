@@ -139,6 +139,7 @@ struct TcParams {
     int32_t ksplit;    // CTAs (one cluster along x) that share a weight slab's K range
     int32_t stages;    // depth of the stage ring, <= kMaxStages
     int32_t *err;
+    int32_t stall_slab;   // test hook: this slab's CTAs never load their first chunk (-1: none)
 };
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -204,8 +205,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     pdl_wait();
 
     if (warp == 0 && lane == 0) {
-        // producer: stage s of round `round` (parity round & 1) waits for the MMAs of round - 1
-        for (int kc = 0, s = 0, round = 0; kc < chunks; ++kc) {
+        // producer: stage s of round `round` (parity round & 1) waits for the MMAs of round - 1.
+        // (Test hook: the stalled slab's producer starts at chunk 1, so stage 0 of round 0 is never armed nor
+        // loaded and the MMA issuer's wait for it runs out.)
+        int kc = 0, s = 0, round = 0;
+        if (n0 == p.stall_slab * kTileN) kc = s = 1;
+        for (; kc < chunks; ++kc) {
             if (round > 0 && !mbar_wait(&empty[s], (round - 1) & 1)) {
                 abort_flag = 1;
                 flag_error(p.err, DR_ERRF_TIMEOUT);
@@ -386,6 +391,7 @@ cudaError_t launch_lm_head_tc(const LmHeadParams &p, int32_t *err, cudaStream_t 
     while (cols < tp.btile) cols <<= 1;
     tp.tmem_cols = cols;
     tp.err = err;
+    tp.stall_slab = p.stall_slab;
     const int ntiles = (p.B + tp.btile - 1) / tp.btile;
     // Split K in two for small batch tiles when the weight slabs alone leave SMs idle; with more CTAs
     // than SMs the ring shrinks so that two CTAs share an SM (one wave).

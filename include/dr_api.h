@@ -298,6 +298,22 @@ dr_status dr_lm_head(const void *hidden, const void *W, int B, int K, int C, int
                      int32_t *err_flag, void *stream);
 
 /*
+ * dr_lm_head_stall_test -- TEST HOOK, never needed in use.  The same call as
+ * dr_lm_head, except that the CTAs of 128-row weight slab `stall_slab` (logit
+ * rows c*V + v in [128*stall_slab, 128*stall_slab + 128)) never load their
+ * first K chunk.  The CTA's bounded pipeline wait for it then runs out (after
+ * about 2 s): DR_ERRF_TIMEOUT is ORed into *err_flag, that slab's logits are
+ * left unwritten, the CTA frees its tensor memory and exits, and every other
+ * logit is written as by dr_lm_head.  Nothing faults or hangs, and later calls
+ * on the same context work normally.  The tests use it to check the failure
+ * path of the waits; the paper has no counterpart.
+ *   B >= 4 (the tensor-core head; DR_ERR_UNSUPPORTED below), 0 <= stall_slab
+ *   < ceil(C*V / 128) (DR_ERR_INVALID_ARG otherwise); the rest as dr_lm_head.
+ */
+dr_status dr_lm_head_stall_test(const void *hidden, const void *W, int B, int K, int C, int V, int ldv, float *logits,
+                                int32_t *err_flag, int stall_slab, void *stream);
+
+/*
  * dr_plan_splits -- host-only query: how many CTAs (one thread-block
  * cluster) share each (b, h) row of an attention call with this batch,
  * head count, length bound and KV storage type (DR_KV_BF16 or

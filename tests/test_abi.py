@@ -134,6 +134,16 @@ def test_split_plan(lib):
     assert plan(0, 16, 4096, BF16, 152) == 1
 
 
+def test_lm_head_stall_hook_validation(lib):
+    # the test hook applies to the tensor-core head (batch >= 4) and to a slab that exists: ceil(9 * 1088 / 128) = 77
+    vp = ctypes.c_void_p
+    call = lambda B=8, slab=0: lib.dr_lm_head_stall_test(vp(FAKE), vp(FAKE), B, 1024, 9, 1088, 1088, vp(FAKE), None,
+                                                       slab, None)
+    assert call(B=3) == 2
+    assert call(slab=-1) == 1
+    assert call(slab=77) == 1
+
+
 @pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++11")])
 def test_header_compiles_alone_as_strict_c_and_cpp(lang, std):
     import shutil

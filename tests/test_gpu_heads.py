@@ -142,3 +142,33 @@ def test_lm_head_feeding_the_sampler(api, cuda_device):
         for c in range(C):
             if clear[b, c] and steps[b] > c:
                 assert np.array_equal(sup_g[b, c], sup_r[b, c]), (b, c)
+
+
+@pytest.mark.parametrize("B", [16, 128])   # K split over a 2-CTA cluster; two batch tiles, K whole
+def test_lm_head_wait_that_runs_out(api, cuda_device, B):
+    # Test hook: the CTAs of weight slab 5 (logit rows 640..767) never load their first K chunk, so their bounded
+    # pipeline wait gives up after about 2 s.  DR_ERRF_TIMEOUT is set, those logits stay unwritten, every other
+    # logit is right, and the next ordinary call on the same context is right everywhere.
+    dev = cuda_device
+    K, C, V = 1024, 9, 1088
+    hidden = W.randn_bf16((B, K), "cpu", 205, B)
+    Wt = (torch.randn((C * V, K), generator=torch.Generator().manual_seed(11)) * (3.0 / K ** 0.5)).to(torch.bfloat16)
+    ref = oracle.lm_head(W.bits(hidden), W.bits(Wt))
+    mag = np.abs(vals(W.bits(hidden))) @ np.abs(vals(W.bits(Wt))).T
+    tol = (K - 1) * 2 * U * mag + 1e-30
+    hd, wd = hidden.to(dev), Wt.to(dev)
+    logits = torch.full((B, C, V), float("nan"), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    api.dr_lm_head_stall_test(hd, wd, C, logits, 5, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & api.DR_ERRF_TIMEOUT
+    got = logits.cpu().numpy().reshape(B, C * V)
+    stalled = np.zeros(C * V, bool)
+    stalled[640:768] = True
+    assert np.isnan(got[:, stalled]).all()
+    assert (np.abs(got[:, ~stalled] - ref[:, ~stalled]) <= tol[:, ~stalled]).all()
+    err.zero_()
+    api.dr_lm_head(hd, wd, C, logits, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert (np.abs(logits.cpu().numpy().reshape(B, C * V) - ref) <= tol).all()
