@@ -146,3 +146,41 @@ def test_fp8_separate_calls_equal_fused(api, cuda_device):
     torch.cuda.synchronize()
     assert torch.equal(kv1.k, kv2.k) and torch.equal(kv1.v, kv2.v)
     assert torch.equal(o1, o2)
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+def test_fp8_fused_layer_edge_lengths(api, cuda_device, layout):
+    # the fused append quantises this step's key inside the attention launch: lengths at and around the 16-key
+    # tile edges, a row of one key, the capacity, and description lengths around the packing threshold
+    dev = cuda_device
+    lens = np.array([1, 2, 16, 17, 64, 255, 256], np.int32)
+    enc_len = np.array([1, 300, 16, 17, 5, 299, 100], np.int32)
+    B = len(lens)
+    w = W.Workload(320, "fp8 edge", 1, B, layout, lens, 256, enc_len, 300, 1.0, 1, 1.0, np.zeros(B, np.uint64),
+                   np.zeros(B, np.int32))
+    c = W.make_self_cache_fp8(w, 0)
+    q, qx, kn, vn = W.make_step_inputs(w, 0)
+    kx, vx = W.make_cross_kv(w, 0)
+    s = default_scale(D)
+    refx = oracle.attn_contiguous(W.bits(qx), W.bits(kx), W.bits(vx), enc_len, s)
+    for hint in (0, 64):
+        kv = dev_cache(api, c, dev)
+        out = torch.empty((B, 16, D), dtype=torch.bfloat16, device=dev)
+        outx = torch.empty_like(out)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        api.dr_decode_layer(q.to(dev), kv, kn.to(dev), vn.to(dev), torch.from_numpy(lens).to(dev), qx.to(dev),
+                            kx.to(dev), vx.to(dev), torch.from_numpy(enc_len).to(dev), out, outx,
+                            max_seq_len_hint=hint, err_flag=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        kh, vh = codes(c.k).copy(), codes(c.v).copy()
+        if layout == "contiguous":
+            oracle.kv_append_fp8_contiguous(kh, vh, W.bits(kn), W.bits(vn), lens - 1, c.k_scale, c.v_scale)
+            ref = oracle.attn_fp8_contiguous(W.bits(q), kh, vh, lens, s, c.k_scale, c.v_scale)
+        else:
+            t = c.block_table.numpy()
+            oracle.kv_append_fp8_paged(kh, vh, t, W.bits(kn), W.bits(vn), lens - 1, c.k_scale, c.v_scale)
+            ref = oracle.attn_fp8_paged(W.bits(q), kh, vh, t, lens, s, c.k_scale, c.v_scale)
+        assert np.array_equal(codes(kv.k), kh) and np.array_equal(codes(kv.v), vh), f"codes, hint {hint}"
+        assert_attn_close(out, ref, f"fp8 fused self {layout} hint {hint}")
+        assert_attn_close(outx, refx, f"fused cross {layout} hint {hint}")
