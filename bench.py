@@ -30,6 +30,7 @@ import re
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -102,39 +103,72 @@ def max_over_ranks(dist, x: float, device) -> float:
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while the timed regions run.
+
+    Entering starts the sampler and waits for its first sample, so that it is already running when the first
+    timed region starts.  A reader thread stamps each sample with its arrival time.  Timed regions much shorter
+    than the sampling interval (batch 1: a few milliseconds) would see no sample at all, so `hold` keeps the GPU
+    busy with untimed replays of the same work until the window has lasted MIN_WINDOW_S; the summary covers
+    the samples of that window (the timed regions plus those replays) and says how long it was."""
+
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 100
+    MIN_WINDOW_S = 0.35
 
     def __init__(self, gpu_index: int):
         self.proc = None
         self.idx = gpu_index
+        self.stamped = []          # (arrival time, line)
+        self.t0 = self.t1 = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.stamped.append((time.perf_counter(), line))
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
+        if self.proc is not None:
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            deadline = time.perf_counter() + 5.0
+            while not self.stamped and time.perf_counter() < deadline and self.proc.poll() is None:
+                time.sleep(0.005)
+        self.t0 = time.perf_counter()
         return self
 
+    def hold(self, replay):
+        """Run `replay()` (untimed, the same work as the timed regions) until the window is MIN_WINDOW_S long."""
+        if self.proc is None:
+            return
+        while time.perf_counter() - self.t0 < self.MIN_WINDOW_S:
+            replay()
+
     def __exit__(self, *exc):
-        self.lines = []
+        self.t1 = time.perf_counter()
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+                self.proc.wait()
+            self.reader.join(timeout=5)
         return False
 
     def summary(self):
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in getattr(self, "lines", []):
+        for t, line in self.stamped:
+            if self.t0 is None or not (self.t0 <= t <= self.t1):
+                continue
             f = [x.strip() for x in line.split(",")]
             if len(f) < 8:
                 continue
@@ -148,7 +182,8 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm),
+                "window_s": round(self.t1 - self.t0, 3)}
 
 
 def measured_peaks():
@@ -600,6 +635,18 @@ def main():
         samp_total_ms = timed("sampler")
         head_total_ms = timed("lm_head")
         emb_total_ms = timed("embed")
+
+        # Regions of a few milliseconds (batch 1) are shorter than the clock sampling interval: keep the GPU on
+        # the same steps (untimed replays, idempotent: same appends, no step advance) until the sampler has seen
+        # them.
+        def replay_steps():
+            if graphs is not None:
+                graphs["step"].replay()
+            else:
+                steps()
+            torch.cuda.synchronize()
+
+        clk.hold(replay_steps)
     barrier(dist)
     ms = max_over_ranks(dist, step_total_ms / K, dev)
     self_avg_ms = self_total_ms / (K * w.layers)
