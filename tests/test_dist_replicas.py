@@ -71,3 +71,24 @@ def test_replicas_draw_distinct_batches():
     a = W.make_step_inputs(w, 1000 * 0 + 0)[0]
     b = W.make_step_inputs(w, 1000 * 1 + 0)[0]
     assert a.shape == b.shape and not torch.equal(a, b)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    # Under torchrun the reference arm (the oracle on the host cores) runs on rank 0 alone; the other rank exits 0
+    # without work, and exactly one JSON line comes out.
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
+           "127.0.0.1", "--master-port", str(_free_port()), os.path.join(root, "bench.py"), "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "0", "--workload", "1"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = lines[0]
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
