@@ -43,9 +43,17 @@ def assert_attn_close(got: torch.Tensor, ref: np.ndarray, what: str = "attention
     return float(err.max())
 
 
-def assert_tokens_match(got: torch.Tensor | np.ndarray, ref: dict, what: str = "tokens"):
+def assert_tokens_match(got: torch.Tensor | np.ndarray, ref: dict, what: str = "tokens",
+                        max_excluded: int | None = None):
+    """Tokens equal wherever the oracle's margin is >= MARGIN_EXCLUSION.  At most max_excluded draws (default:
+    1% of all draws, at least 1) may fall under the exclusion, so that a comparison cannot pass by skipping."""
     g = got.cpu().numpy() if isinstance(got, torch.Tensor) else np.asarray(got)
     compare = ref["margins"] >= MARGIN_EXCLUSION
+    n_excl = int((~compare).sum())
+    limit = max(1, compare.size // 100) if max_excluded is None else max_excluded
+    if n_excl > limit:
+        raise AssertionError(f"{what}: {n_excl} of {compare.size} draws fall under the margin exclusion "
+                             f"(at most {limit} allowed)")
     mism = compare & (g != ref["tokens"])
     if mism.any():
         idx = np.argwhere(mism)[:5]

@@ -9,7 +9,10 @@ under the delayed pattern, architecture overview) is pinned by:
   * temperature identities (T=1 and powers of two are exact);
   * the delay-pattern invariant;
   * a chi-squared test that the Gumbel-max draw follows softmax over the top-k set;
-  * softmax probabilities summing to one on exactly the top-k support.
+  * softmax probabilities summing to one on exactly the top-k support;
+  * the Gumbel margin, by behaviour: raising another member of the top-k set
+    by just more than the margin hands the draw to some member, by just less
+    it changes nothing (no score is recomputed here).
 """
 import itertools
 import math
@@ -201,3 +204,58 @@ def test_invalid_inputs_are_rejected():
     x[3] = np.nan
     with pytest.raises(ValueError):
         oracle.sample_row(x, 1.0, 3, 0, 0, 0, 4, -1)
+
+
+def _raised(x: np.float32, delta: float, above: bool) -> np.float32:
+    """The float32 nearest x + delta whose exact increase over x is at least delta (above) or at most delta."""
+    y = np.float32(float(x) + delta)
+    step = np.float32(np.inf if above else -np.inf)
+    while (float(y) - float(x) < delta) if above else (float(y) - float(x) > delta):
+        y = np.nextafter(y, step, dtype=np.float32)
+    return y
+
+
+def _margin_row(rng, V, k, ties):
+    x = (rng.normal(size=V) * 3).astype(np.float32)
+    if ties:   # entries that share the value of the k-th largest: ties at the top-k boundary
+        kth = np.argsort(-x, kind="stable")[k - 1]
+        x[rng.choice(V, size=min(V - 1, 6), replace=False)] = x[kth]
+    return x
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5])
+@pytest.mark.parametrize("V,k", [(8, 2), (8, 5), (64, 2), (64, 50), (1088, 2), (1088, 50), (1088, 250)])
+@pytest.mark.parametrize("ties", [False, True])
+def test_gumbel_margin_is_the_gap_to_the_runner_up(V, k, T, ties):
+    """The margin m the oracle returns is the gap between the best and the second-best perturbed score.
+
+    Checked through the draw alone: only member i's score moves when its logit is raised (its uniform is
+    indexed by vocabulary id, and a member stays a member), and by exactly the raise of x_i = logit_i / T
+    (T = 1, or T = 0.5 where the division is exact).  So raising some member by more than m must hand the
+    draw to it -- the runner-up -- and raising any member by less than m must leave the draw where it was.
+    A margin that is too large fails the second half (the runner-up overtakes early), one that is too small
+    the first (nobody overtakes)."""
+    rng = np.random.default_rng(V * 1000 + k + (7 if ties else 0) + int(T * 10))
+    compared = 0
+    for trial in range(3 if V == 1088 else 10):
+        x = _margin_row(rng, V, k, ties)
+        seed, b, c, step = int(rng.integers(0, 2 ** 63)), trial, trial % 9, 20 + trial
+        draw = lambda y: oracle.sample_row(y, T, k, seed, b, c, step, -1)["token"]
+        r = oracle.sample_row(x, T, k, seed, b, c, step, -1, want_topk=True)
+        t, m = r["token"], r["margin"]
+        assert draw(x) == t
+        if not (0.0 < m < math.inf):
+            continue
+        compared += 1
+        overtaken = []
+        for i in (int(j) for j in r["topk"] if j != t):
+            y = x.copy()
+            y[i] = _raised(x[i], T * m * (1 + 1e-6), above=True)
+            got = draw(y)
+            assert got in (t, i), (i, got)            # a raise of i can only hand the draw to i
+            if got == i:
+                overtaken.append(i)
+            y[i] = _raised(x[i], T * m * (1 - 1e-6), above=False)
+            assert draw(y) == t, (i, m)               # just short of the margin: no change
+        assert overtaken, ("no member overtakes the draw with a raise of the margin", m)
+    assert compared >= 2
