@@ -276,6 +276,8 @@ dr_status dr_embed_tokens(const int32_t *tokens, const void *table, int B, int C
     if (!tokens || !table || !out || !aligned16(table) || !aligned16(out)) return DR_ERR_INVALID_ARG;
     if (B < 1 || B > 0x7FFFFFFF || C < 1 || V < 1 || Dm < 8 || Dm % 8 != 0) return DR_ERR_INVALID_ARG;
     if (out_dtype != DR_BF16 && out_dtype != DR_F32) return DR_ERR_INVALID_ARG;
+    // the kernel keeps one token per codebook in registers, up to kMaxCodebooks of them
+    if (C > dr::kMaxCodebooks) return DR_ERR_UNSUPPORTED;
     dr::EmbedParams p;
     p.tokens = tokens;
     p.table = static_cast<const uint16_t *>(table);

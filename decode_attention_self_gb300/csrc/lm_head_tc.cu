@@ -253,6 +253,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         mma_commit(&done);
     }
     __syncwarp();
+    // The producer and the MMA issuer set abort_flag with plain shared stores; this barrier orders them before
+    // the epilogue reads it, so that every warp of the CTA takes the same decision to write or not.
+    __syncthreads();
 
     pdl_trigger();
     // epilogue: warp w owns TMEM lanes (W rows) 32w .. 32w+31

@@ -285,7 +285,9 @@ __global__ void __launch_bounds__(kThreads, kThreads == kNarrowThreads ? 8 : kWi
                     bs = s_rf[w];
                     bi = s_ri[w];
                 }
-            p.tokens[(size_t)b * p.C + c] = bi;
+            // NaN scores are never `better`: a set of NaN members alone leaves bi at its start value.  The
+            // token is then undefined but stays a member of the kept set, so it is in range.
+            p.tokens[(size_t)b * p.C + c] = bi == 0x7FFFFFFF ? s_list[0] : bi;
         }
 
         // ---- optional softmax over the kept set -------------------------------

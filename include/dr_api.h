@@ -263,6 +263,7 @@ dr_status dr_sample_topk_delayed(const float *logits, int B, int C, int V, int l
  * optimizations item 3: the nine codebook embedding lookups merged into one
  * (one merged table, one gather of C rows per batch row).
  *
+ *   C      : codebooks, 1..16 (DR_ERR_UNSUPPORTED above 16, as for the sampler)
  *   tokens : [B][C] int32 (device), e.g. the tokens dr_sample_topk_delayed wrote
  *   table  : [C*V][Dm] bf16 (device, 16-byte aligned); codebook c's rows start at c*V
  *   out    : [B][Dm] in out_dtype (device, 16-byte aligned); fp32 sum in c order

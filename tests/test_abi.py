@@ -118,6 +118,23 @@ def test_sampler_validation(lib):
                                       None) == 1
 
 
+def test_embedding_validation(lib):
+    # the merged embedding lookup keeps one token per codebook on chip, for up to 16 codebooks: a 17th is refused
+    # before anything is enqueued rather than left out of the sum
+    vp = ctypes.c_void_p
+    call = lambda B=2, C=9, V=1088, Dm=1024, od=0, tok=FAKE, table=FAKE, out=FAKE: lib.dr_embed_tokens(
+        vp(tok) if tok else None, vp(table) if table else None, B, C, V, Dm, vp(out) if out else None, od, None, None)
+    assert call(C=17) == 2
+    assert call(C=64) == 2
+    assert call(C=0) == 1
+    assert call(B=0) == 1
+    assert call(V=0) == 1
+    assert call(Dm=12) == 1                       # not a multiple of 8
+    assert call(od=5) == 1
+    assert call(tok=0) == 1
+    assert call(table=FAKE + 8) == 1              # table must be 16-byte aligned
+
+
 def test_split_plan(lib):
     # split count per (b, h) row: one cluster of at most 8 CTAs, >= 64 keys each, <= 256 KiB of K+V each at
     # the longest row, and at least 6 CTAs per SM of a 152-SM GPU when the rows alone are fewer.

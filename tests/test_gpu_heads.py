@@ -32,13 +32,14 @@ def vals(b):
     return torch.from_numpy(b.astype(np.int16)).view(torch.bfloat16).double().numpy()
 
 
-@pytest.mark.parametrize("B", [1, 5, 128])
+@pytest.mark.parametrize("B,C", [(1, 9), (5, 9), (128, 9), (3, 16), (130, 16), (2, 1)])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-def test_embed_tokens(api, cuda_device, B, out_dtype):
+def test_embed_tokens(api, cuda_device, B, C, out_dtype):
+    # C = 16 is the largest codebook count the call accepts: every one of the 16 rows enters the sum
     dev = cuda_device
-    C, V, Dm = 9, 1088, 1024
-    table = W.randn_bf16((C * V, Dm), "cpu", 200, 1)
-    tokens = torch.from_numpy(np.random.default_rng(B).integers(0, V, size=(B, C)).astype(np.int32))
+    V, Dm = 1088, 1024
+    table = W.randn_bf16((C * V, Dm), "cpu", 200, C)
+    tokens = torch.from_numpy(np.random.default_rng(B + 1000 * C).integers(0, V, size=(B, C)).astype(np.int32))
     out = torch.empty((B, Dm), dtype=out_dtype, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     api.dr_embed_tokens(tokens.to(dev), table.to(dev), V, out, err_flag=err)
@@ -49,6 +50,18 @@ def test_embed_tokens(api, cuda_device, B, out_dtype):
     mag = np.stack([sum(tv[c * V + int(tokens[b, c])] for c in range(C)) for b in range(B)])
     tol = C * U * mag + (2.0 ** -8 * np.abs(ref) if out_dtype == torch.bfloat16 else 0)
     assert (np.abs(out.float().cpu().numpy() - ref) <= tol + 1e-30).all()
+
+
+def test_embed_more_than_16_codebooks_is_refused(api, cuda_device):
+    dev = cuda_device
+    C, V, Dm = 17, 8, 64
+    table = torch.zeros((C * V, Dm), dtype=torch.bfloat16, device=dev)
+    tokens = torch.zeros((2, C), dtype=torch.int32, device=dev)
+    out = torch.full((2, Dm), 7.0, dtype=torch.float32, device=dev)
+    with pytest.raises(RuntimeError, match="unsupported"):
+        api.dr_embed_tokens(tokens, table, V, out)
+    torch.cuda.synchronize()
+    assert (out == 7.0).all()                     # nothing was enqueued
 
 
 def test_embed_invalid_token_is_left_out_and_flagged(api, cuda_device):

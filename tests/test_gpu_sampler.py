@@ -269,3 +269,20 @@ def test_positive_infinity_and_a_tiny_temperature(api, cuda_device):
     tok, _, _ = run_gpu(api, dev, y, float(T), 50, seeds, steps, 1024, want_probs=False)
     ref = oracle.sample(y, float(T), 50, seeds, steps, 1024)
     assert np.array_equal(tok.cpu().numpy(), first) and np.array_equal(ref["tokens"], first)
+
+
+@pytest.mark.parametrize("k", [1, 3, 50])
+def test_nan_logits_token_stays_in_range(api, cuda_device, k):
+    # NaN logits have no defined draw (the oracle refuses them), but the token must stay inside [0, V): a NaN
+    # order key sorts above +inf, so with top_k = 1 the kept set can be a NaN entry alone, and then every
+    # perturbed score of the set is NaN.
+    rng = np.random.default_rng(80 + k)
+    B, C, V = 3, 9, 300
+    x = (rng.normal(size=(B, C, V)) * 3).astype(np.float32)
+    x[0, :, 17] = np.nan                               # one NaN per row
+    x[1, :, ::50] = np.nan                             # several
+    x[2, :, :] = np.nan                                # all of them
+    tok, _, _ = run_gpu(api, cuda_device, x, 1.0, k, np.arange(B, dtype=np.uint64), np.full(B, 20, np.int32),
+                        1024, want_probs=False)
+    t = tok.cpu().numpy()
+    assert ((t >= 0) & (t < V)).all(), t
