@@ -225,20 +225,34 @@ def committed_traffic(kernel_key: str):
 # ---------------------------------------------------------------------------
 class DeviceStep:
     """One decode step on the GPU: per layer one fused dr_decode_layer launch (append + self + cross), or with
-    fused=False the three separate calls; then dr_sample_topk_delayed once."""
+    fused=False the three separate calls; then dr_sample_topk_delayed once.
 
-    def __init__(self, w: W.Workload, dev, rank: int, fused: bool = True, fp8: bool = False):
+    copies > 1 keeps that many copies of every layer's buffers (caches, description K/V, step inputs) at
+    different addresses, and step i uses copy i % copies: a step then finds none of its data in L2 from the
+    previous step when one step's bytes are below the L2 size (batch 1)."""
+
+    def __init__(self, w: W.Workload, dev, rank: int, fused: bool = True, fp8: bool = False, copies: int = 1):
         from decode_attention_self_gb300 import api
 
-        self.api, self.w, self.dev, self.fused = api, w, dev, fused
-        self.layers = []
+        self.api, self.w, self.dev, self.fused, self.copies = api, w, dev, fused, copies
+        base = []
         for l in range(w.layers):
             c = (W.make_self_cache_fp8 if fp8 else W.make_self_cache)(w, 1000 * rank + l, device=dev)
-            kv = api.KVCache(c.k, c.v, c.block_table.to(dev) if c.block_table is not None else None, c.k_scale,
-                             c.v_scale)
             kx, vx = W.make_cross_kv(w, 1000 * rank + l, device=dev)
             q, qx, kn, vn = W.make_step_inputs(w, 1000 * rank + l, device=dev)
-            self.layers.append(dict(kv=kv, kx=kx, vx=vx, q=q, qx=qx, kn=kn, vn=vn))
+            base.append(dict(c=c, kx=kx, vx=vx, q=q, qx=qx, kn=kn, vn=vn))
+        self.sets = []
+        for cp in range(copies):
+            layers = []
+            for b in base:
+                t = {k: (v if cp == 0 else v.clone()) for k, v in b.items() if k != "c"}
+                c = b["c"]
+                k, v = (c.k, c.v) if cp == 0 else (c.k.clone(), c.v.clone())
+                table = c.block_table.to(dev) if c.block_table is not None else None
+                t["kv"] = api.KVCache(k, v, table, c.k_scale, c.v_scale)
+                layers.append(t)
+            self.sets.append(layers)
+        self.layers = self.sets[0]
         self.pos = torch.from_numpy(w.seq_len - 1).to(dev)
         self.seq = torch.from_numpy(w.seq_len).to(dev)
         self.enc = torch.from_numpy(w.enc_len).to(dev)
@@ -250,9 +264,13 @@ class DeviceStep:
         self.out_x = torch.empty_like(self.out_s)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.hint = int(w.seq_len.max())
-        # the decoder's output and input ends (not part of the timed step): merged LM head and
-        # merged embedding lookup, synthetic weights [C*V, 1024] bf16.  HEAD_COPIES distinct copies of
-        # each (160 MB in all, more than L2) are used in turn, so every call reads its weights from HBM.
+        self.hidden = self.w_head = self.w_emb = None
+
+    def make_decoder_ends(self, rank: int = 0):
+        """The decoder's output and input ends (not part of the timed step): merged LM head and merged
+        embedding lookup, synthetic weights [C*V, 1024] bf16.  HEAD_COPIES distinct copies of each (160 MB in
+        all, more than L2) are used in turn, so every call reads its weights from HBM."""
+        w, dev = self.w, self.dev
         self.hidden = W.randn_bf16((w.B, 1024), dev, w.index, 500 + rank)
         self.w_head = [(W.randn_bf16((w.C * w.V, 1024), dev, w.index, 501 + 2 * i) * 0.1).contiguous()
                        for i in range(HEAD_COPIES)]
@@ -271,9 +289,9 @@ class DeviceStep:
     def launches_per_step(self) -> int:
         return (1 if self.fused else 3) * self.w.layers + 1
 
-    def run_layer(self, l, seq=None, pos=None):
+    def run_layer(self, l, seq=None, pos=None, copy: int = 0):
         """Layer l of the step; seq/pos (device int32 [B]) default to the workload's lengths."""
-        api, L = self.api, self.layers[l]
+        api, L = self.api, self.sets[copy % self.copies][l]
         seq = self.seq if seq is None else seq
         pos = self.pos if pos is None else pos
         if self.fused:
@@ -285,23 +303,27 @@ class DeviceStep:
                                     err_flag=self.err)
             api.dr_decode_cross_attn(L["qx"], L["kx"], L["vx"], self.enc, self.out_x[l], err_flag=self.err)
 
-    def run_dominant(self):
-        """The dominant kernel's launches of one step: the fused layer launches, or the self-attention calls."""
-        for l, L in enumerate(self.layers):
+    def run_dominant(self, i: int = 0):
+        """The dominant kernel's launches of step i: the fused layer launches, or the self-attention calls."""
+        for l in range(self.w.layers):
             if self.fused:
-                self.run_layer(l)
+                self.run_layer(l, copy=i)
             else:
-                self.api.dr_decode_self_attn(L["q"], L["kv"], self.seq, self.out_s[l], max_seq_len_hint=self.hint,
-                                             err_flag=self.err)
+                self.run_self_attn(l, i)
+
+    def run_self_attn(self, l: int, i: int = 0):
+        L = self.sets[i % self.copies][l]
+        self.api.dr_decode_self_attn(L["q"], L["kv"], self.seq, self.out_s[l], max_seq_len_hint=self.hint,
+                                     err_flag=self.err)
 
     def run_sampler_only(self):
         w = self.w
         self.api.dr_sample_topk_delayed(self.logits, w.temperature, w.top_k, self.seeds, self.step, w.pad_id,
                                         self.tokens, V=w.V)
 
-    def run(self):
+    def run(self, i: int = 0):
         for l in range(self.w.layers):
-            self.run_layer(l)
+            self.run_layer(l, copy=i)
         self.run_sampler_only()
 
 
@@ -309,7 +331,9 @@ def time_long_output(ds: DeviceStep, kv_bytes: int, start: int = 0, chunk: int =
     """The long-output run itself (batch 1): n_steps consecutive steps, step t appending key start + t of every
     layer, attending start + t + 1 keys and sampling with the device step counter advancing.  Captured as
     graphs of `chunk` steps (the lengths come from a device array, one element per step) and replayed back to
-    back between two events.  Overwrites the caches' keys start .. start + n_steps - 1."""
+    back between two events.  Overwrites the caches' keys start .. start + n_steps - 1.  With ds.copies > 1,
+    step t appends into and attends over copy t % copies of the layers' buffers: every step moves the same
+    bytes, and none of them stay in L2 from the step before."""
     w, api, dev = ds.w, ds.api, ds.dev
     assert w.B == 1 and w.n_steps > 1 and start + w.n_steps <= w.cap
     T = w.n_steps
@@ -326,7 +350,7 @@ def time_long_output(ds: DeviceStep, kv_bytes: int, start: int = 0, chunk: int =
         with torch.cuda.graph(g, stream=cs):
             for t in range(t0, min(T, t0 + chunk)):
                 for l in range(w.layers):
-                    ds.run_layer(l, seq=lens[t:t + 1], pos=pos_all[t:t + 1])
+                    ds.run_layer(l, seq=lens[t:t + 1], pos=pos_all[t:t + 1], copy=t)
                 api.dr_sample_topk_delayed(ds.logits, w.temperature, w.top_k, ds.seeds, step, w.pad_id, ds.tokens,
                                            V=w.V, advance=True)
         torch.cuda.current_stream().wait_stream(cs)
@@ -518,6 +542,194 @@ def time_oracle_one_thread(min_seconds: float = 0.5) -> dict:
 
 
 # ---------------------------------------------------------------------------
+# one workload, measured on the GPU
+# ---------------------------------------------------------------------------
+SUB_WORKLOADS = ("1", "2", "3", "4", "4e", "5e")   # measured after the headline workload in the default run
+
+
+def rotation_copies(step_b: int) -> int:
+    """Copies of the layers' buffers a step rotates through so that the bytes between two uses of the same
+    buffer are at least 3x L2; 1 when one step already is, or when it would take more than 8 copies (a step
+    far smaller than L2, whose figure is then a warm-L2 one)."""
+    if step_b >= 3 * L2_BYTES:
+        return 1
+    n = math.ceil(3 * L2_BYTES / step_b)
+    return n if n <= 8 else 1
+
+
+def l2_note(step_b: int, copies: int) -> str:
+    if copies > 1:
+        return (f"{copies} copies of every layer's caches and inputs used in turn: {copies * step_b / 1e6:.0f} MB "
+                f"between two uses of the same data (>= 3x the 129 MB L2)")
+    if step_b > L2_BYTES:
+        return "inputs larger than L2 (%.1f GB per step vs 129 MB)" % (step_b / 1e9)
+    return "inputs smaller than L2 (%.2f MB per step): warm-L2 figure" % (step_b / 1e6)
+
+
+def workload_config(w: W.Workload, sb: dict, fp8: bool, ws: int, copies: int) -> dict:
+    return {"workload": f"{w.index}: {w.name}", "batch": w.B, "layers": w.layers,
+            "heads": w.H, "head_dim": w.D, "kv_layout": w.layout, "kv_dtype": "e4m3" if fp8 else "bf16",
+            "codebooks": w.C, "vocab": w.V, "top_k": w.top_k, "temperature": w.temperature,
+            "self_len_mean": float(w.seq_len.mean()), "self_len_max": int(w.seq_len.max()),
+            "cross_len_mean": float(w.enc_len.mean()), "parallelism": f"replicas x{ws}",
+            "bytes_per_step": sb["step"], "l2": l2_note(sb["step"], copies)}
+
+
+def measure(w: W.Workload, K: int, warmup: int, dev, rank: int, ws: int, dist, *, fused=True, fp8=False,
+            copies=1, eager=False, decoder_ends=False, standalone_self=False, e2e=False, long_output=False,
+            gpu_index=0) -> dict:
+    """Time K decode steps of workload w (and the dominant kernel, the sampler and the optional extras on their
+    own), with an nvidia-smi clock record over the timed regions."""
+    kvb = 1 if fp8 else 2
+    sb = step_bytes(w, kv_bytes=kvb)
+    ds = DeviceStep(w, dev, rank, fused=fused, fp8=fp8, copies=copies)
+    if decoder_ends:
+        ds.make_decoder_ends(rank)
+    torch.cuda.synchronize()
+    for i in range(max(3, warmup)):
+        ds.run(i)
+    torch.cuda.synchronize()
+    assert int(ds.err.item()) == 0, "device error flag set during warm-up"
+    K = max(K, copies) // copies * copies   # every copy is used equally often
+
+    # The timed region is K decode steps, captured as one CUDA graph (the page's own way of removing launch
+    # overhead) with no event nodes inside it; eager launches them one by one.  The dominant kernel's average
+    # launch duration is then timed the same way on its own: a graph of its K x layers launches of the timed
+    # steps, back to back (same arguments), bracketed by events; likewise the sampler's K launches.
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream()
+        cs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cs):
+            fn()
+        torch.cuda.current_stream().wait_stream(cs)
+        g.replay()                                         # untimed: instantiation and first-touch costs
+        torch.cuda.synchronize()
+        return g
+
+    regions = {"step": lambda: [ds.run(i) for i in range(K)],
+               "dominant": lambda: [ds.run_dominant(i) for i in range(K)],
+               "sampler": lambda: [ds.run_sampler_only() for _ in range(K)]}
+    if decoder_ends:
+        regions["lm_head"] = lambda: [ds.run_lm_head(i) for i in range(K)]
+        regions["embed"] = lambda: [ds.run_embed(i) for i in range(K)]
+    if standalone_self and fused:
+        regions["self_attn"] = lambda: [ds.run_self_attn(l, i) for i in range(K) for l in range(w.layers)]
+    graphs = None if eager else {k: capture(f) for k, f in regions.items()}
+
+    def timed(name):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0.record()
+        if graphs is not None:
+            graphs[name].replay()
+        else:
+            regions[name]()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    with ClockSampler(gpu_index) as clk:
+        t_ms = {name: timed(name) for name in regions}
+
+        # Regions of a few milliseconds (batch 1) are shorter than the clock sampling interval: keep the GPU on
+        # the same steps (untimed replays, idempotent: same appends, no step advance) until the sampler has seen
+        # them.
+        def replay_steps():
+            if graphs is not None:
+                graphs["step"].replay()
+            else:
+                regions["step"]()
+            torch.cuda.synchronize()
+
+        clk.hold(replay_steps)
+    barrier(dist)
+    ms = max_over_ranks(dist, t_ms["step"] / K, dev)
+    dom_ms = t_ms["dominant"] / (K * w.layers)
+    peaks, peak_kind = measured_peaks()
+    dom_bytes = sb["self"] + sb["cross"] + sb["append"] if fused else sb["self"]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    kname = "decode_attn_kernel<fused>" if fused else "decode_attn_kernel"
+    traffic = committed_traffic(f"{kname} workload {w.index} {'e4m3' if fp8 else 'bf16'}")
+    drawing = int(sum(int(w.steps[b]) > c for b in range(w.B) for c in range(w.C)))
+    r = {"value": sb["step"] * ws / (ms * 1e-3) / 1e9, "ms_per_step": ms, "us_per_step": ms * 1e3,
+         "layer_us" if fused else "self_attn_us": dom_ms * 1e3,
+         "sampler_us": t_ms["sampler"] / K * 1e3, "sampler_draws": drawing,
+         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": achieved / peaks["hbm_gbs"],
+                      "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
+                      "kernel": kname + (" (dr_decode_layer: append + self + cross)" if fused
+                                         else " (dr_decode_self_attn)"),
+                      "peak_kind": peak_kind, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                      "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_us": dom_ms * 1e3},
+         "config": workload_config(w, sb, fp8, ws, copies), "steps": K,
+         "gpu_launches": ds.launches_per_step() * K, "launch_mode": "eager" if eager else "cuda_graph"}
+    if "self_attn" in t_ms:
+        sa_ms = t_ms["self_attn"] / (K * w.layers)
+        sa = sb["self"] / (sa_ms * 1e-3) / 1e9
+        r["self_attn_standalone"] = {"us": sa_ms * 1e3, "achieved": sa, "frac": sa / peaks["hbm_gbs"],
+                                     "frac_of_nominal_8tbs": sa / NOMINAL_HBM_GBS,
+                                     "algorithmic_bytes_per_launch": sb["self"],
+                                     "kernel": "decode_attn_kernel (dr_decode_self_attn)"}
+    if decoder_ends:
+        r["decoder_ends"] = {
+            "lm_head": {"us": t_ms["lm_head"] / K * 1e3, "batch": w.B, "K": 1024, "N": w.C * w.V,
+                        "weight_GBps": w.C * w.V * 1024 * 2 / (t_ms["lm_head"] / K * 1e-3) / 1e9,
+                        "weights": f"{HEAD_COPIES} copies used in turn (more than L2)"},
+            "embed": {"us": t_ms["embed"] / K * 1e3, "rows_gathered": w.B * w.C, "Dm": 1024,
+                      "tables": f"{HEAD_COPIES} copies used in turn (more than L2)"}}
+    r["clocks"] = clk.summary()
+
+    if e2e:
+        # End to end: every step copies its inputs in from pinned host memory and its tokens back out, the next
+        # step's copies overlapping this step's kernels.  In graph mode the K steps, with their copies on a
+        # second stream, are one graph replayed once.
+        hs = HostStep(ds)
+        hs.run_steps(2)
+        torch.cuda.synchronize()
+        g_e2e = capture(lambda: hs.run_steps(K)) if graphs is not None else None
+        barrier(dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        if g_e2e is not None:
+            g_e2e.replay()
+        else:
+            hs.run_steps(K)
+        e1.record()
+        torch.cuda.synchronize()
+        ems = max_over_ranks(dist, e0.elapsed_time(e1) / K, dev)
+        r["e2e"] = {"value": sb["step"] * ws / (ems * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems,
+                    "h2d_bytes_per_step": hs.h2d, "d2h_bytes_per_step": hs.d2h,
+                    "mode": ("cuda_graph with copy nodes" if g_e2e is not None else "eager") +
+                            ", one input copy per step, inputs and tokens double-buffered: copies overlap the "
+                            "previous step"}
+
+    # the long-output workload: also the whole growing run, not only its last (longest) step, and the same
+    # number of steps growing from there to the cache's capacity
+    if long_output and w.n_steps > 1 and not eager:
+        with ClockSampler(gpu_index) as clk2:
+            lo = time_long_output(ds, kv_bytes=kvb)
+            if 2 * w.n_steps <= w.cap:
+                lo["continued"] = time_long_output(ds, kv_bytes=kvb, start=w.n_steps)
+        lo["clocks"] = clk2.summary()
+        lo["l2"] = (f"{copies} copies of every layer's caches used in turn" if copies > 1 else "one copy")
+        r["long_output"] = lo
+
+    assert int(ds.err.item()) == 0, "device error flag set during the timed steps"
+    del ds, graphs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return r
+
+
+def sub_workload(name: str):
+    """'4' -> workload 4 with a bf16 cache; '4e' -> the same with an e4m3 cache."""
+    return int(name.rstrip("e")), name.endswith("e")
+
+
+# ---------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -533,18 +745,21 @@ def main():
                     help="self-attention cache format (fp8 = OCP E4M3 codes with per-layer scales)")
     ap.add_argument("--unfused", action="store_true",
                     help="three launches per layer (append, self, cross) instead of one dr_decode_layer launch")
+    ap.add_argument("--copies", type=int, default=0,
+                    help="copies of the layers' buffers rotated over the steps (0: enough for 3x L2 at batch 1)")
+    ap.add_argument("--sub", default="auto",
+                    help="workloads measured after the headline one, comma-separated ('4e' = workload 4 with an "
+                         "e4m3 cache); 'auto': %s after the default workload 5 run, none otherwise; 'none'"
+                         % ",".join(SUB_WORKLOADS))
     args = ap.parse_args()
     ws, rank, local = dist_env()
     w = W.make_workload(args.workload)
     if args.layers > 0:
         w = dataclasses.replace(w, layers=args.layers)
-    sb = step_bytes(w, kv_bytes=1 if args.kv == "fp8" else 2)
-    config = {"workload": f"{w.index}: {w.name}", "batch": w.B, "layers": w.layers,
-              "heads": w.H, "head_dim": w.D, "kv_layout": w.layout, "kv_dtype": "e4m3" if args.kv == "fp8" else "bf16", "codebooks": w.C,
-              "vocab": w.V, "top_k": w.top_k, "temperature": w.temperature,
-              "self_len_mean": float(w.seq_len.mean()), "self_len_max": int(w.seq_len.max()),
-              "cross_len_mean": float(w.enc_len.mean()), "parallelism": f"replicas x{ws}",
-              "bytes_per_step": sb["step"]}
+    fp8 = args.kv == "fp8"
+    sb = step_bytes(w, kv_bytes=1 if fp8 else 2)
+    copies = args.copies if args.copies > 0 else rotation_copies(sb["step"])
+    config = workload_config(w, sb, fp8, ws, copies)
 
     if args.impl == "reference":
         if rank != 0:
@@ -566,137 +781,28 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist = init_dist(ws, "nccl")
-    ds = DeviceStep(w, dev, rank, fused=not args.unfused, fp8=args.kv == "fp8")
-    torch.cuda.synchronize()
 
-    for _ in range(max(3, args.warmup)):
-        ds.run()
-    torch.cuda.synchronize()
-    assert int(ds.err.item()) == 0, "device error flag set during warm-up"
+    head = measure(w, args.steps, args.warmup, dev, rank, ws, dist, fused=not args.unfused, fp8=fp8,
+                   copies=copies, eager=args.eager, decoder_ends=True, e2e=not args.no_e2e,
+                   long_output=True, gpu_index=local)
 
-    # The timed region is K decode steps, captured as one CUDA graph (the page's own way of
-    # removing launch overhead) with no event nodes inside it; --eager launches them one by one.
-    # The dominant kernel's average launch duration is then timed the same way on its own:
-    # a graph of its K x layers launches of the timed steps, back to back (same arguments),
-    # bracketed by events; likewise the sampler's K launches.
-    K = args.steps
-    mode = "eager" if args.eager else "cuda_graph"
-
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        cs = torch.cuda.Stream()
-        cs.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.graph(g, stream=cs):
-            fn()
-        torch.cuda.current_stream().wait_stream(cs)
-        g.replay()                                         # untimed: instantiation and first-touch costs
-        torch.cuda.synchronize()
-        return g
-
-    def steps():
-        for _ in range(K):
-            ds.run()
-
-    def self_only():
-        for _ in range(K):
-            ds.run_dominant()
-
-    def sampler_only():
-        for _ in range(K):
-            ds.run_sampler_only()
-
-    def head_only():
-        for i in range(K):
-            ds.run_lm_head(i)
-
-    def embed_only():
-        for i in range(K):
-            ds.run_embed(i)
-
-    regions = {"step": steps, "self": self_only, "sampler": sampler_only, "lm_head": head_only, "embed": embed_only}
-    graphs = {k: capture(f) for k, f in regions.items()} if not args.eager else None
-
-    def timed(name):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(dist)
-        torch.cuda.synchronize()
-        e0.record()
-        if graphs is not None:
-            graphs[name].replay()
-        else:
-            regions[name]()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1)
-
-    with ClockSampler(local) as clk:
-        step_total_ms = timed("step")
-        self_total_ms = timed("self")
-        samp_total_ms = timed("sampler")
-        head_total_ms = timed("lm_head")
-        emb_total_ms = timed("embed")
-
-        # Regions of a few milliseconds (batch 1) are shorter than the clock sampling interval: keep the GPU on
-        # the same steps (untimed replays, idempotent: same appends, no step advance) until the sampler has seen
-        # them.
-        def replay_steps():
-            if graphs is not None:
-                graphs["step"].replay()
-            else:
-                steps()
-            torch.cuda.synchronize()
-
-        clk.hold(replay_steps)
-    barrier(dist)
-    ms = max_over_ranks(dist, step_total_ms / K, dev)
-    self_avg_ms = self_total_ms / (K * w.layers)
-    samp_avg_ms = samp_total_ms / K
-    value = sb["step"] * ws / (ms * 1e-3) / 1e9
-
-    peaks, peak_kind = measured_peaks()
-    dom_bytes = sb["self"] + sb["cross"] + sb["append"] if ds.fused else sb["self"]
-    achieved = dom_bytes / (self_avg_ms * 1e-3) / 1e9
-    kname = "decode_attn_kernel<fused>" if ds.fused else "decode_attn_kernel"
-    traffic = committed_traffic(f"{kname} workload {w.index} {'e4m3' if args.kv == 'fp8' else 'bf16'}")
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
-                "kernel": kname + (" (dr_decode_layer: append + self + cross)" if ds.fused else " (dr_decode_self_attn)"),
-                "peak_kind": peak_kind, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
-                "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_us": self_avg_ms * 1e3}
-
-    e2e = None
-    if not args.no_e2e:
-        # End to end: every step copies its inputs in from pinned host memory and its tokens back out,
-        # the next step's copies overlapping this step's kernels.  In graph mode the K steps, with their
-        # copies on a second stream, are one graph replayed once.
-        hs = HostStep(ds)
-        hs.run_steps(2)
-        torch.cuda.synchronize()
-        g_e2e = capture(lambda: hs.run_steps(K)) if graphs is not None else None
-        barrier(dist)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record()
-        if g_e2e is not None:
-            g_e2e.replay()
-        else:
-            hs.run_steps(K)
-        e1.record()
-        torch.cuda.synchronize()
-        ems = max_over_ranks(dist, e0.elapsed_time(e1) / K, dev)
-        e2e = {"value": sb["step"] * ws / (ems * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems,
-               "h2d_bytes_per_step": hs.h2d, "d2h_bytes_per_step": hs.d2h,
-               "mode": ("cuda_graph with copy nodes" if g_e2e is not None else "eager") +
-                       ", one input copy per step, inputs and tokens double-buffered: copies overlap the previous step"}
-
-    # the long-output workload: also the whole growing run, not only its last (longest) step, and the same
-    # number of steps growing from there to the cache's capacity
-    long_output = None
-    if w.n_steps > 1 and not args.eager:
-        kvb = 1 if args.kv == "fp8" else 2
-        long_output = time_long_output(ds, kv_bytes=kvb)
-        if 2 * w.n_steps <= w.cap:
-            long_output["continued"] = time_long_output(ds, kv_bytes=kvb, start=w.n_steps)
+    if args.sub == "auto":
+        subs = list(SUB_WORKLOADS) if args.workload == 5 and args.layers == 0 and not args.unfused else []
+    else:
+        subs = [x for x in args.sub.split(",") if x and x != "none"]
+    sub = {}
+    for name in subs:
+        idx, sfp8 = sub_workload(name)
+        sw = W.make_workload(idx)
+        scopies = rotation_copies(step_bytes(sw, kv_bytes=1 if sfp8 else 2)["step"])
+        r = measure(sw, args.steps, args.warmup, dev, rank, ws, dist, fp8=sfp8, copies=scopies, eager=args.eager,
+                    standalone_self=idx == 4, long_output=idx == 3, gpu_index=local)
+        sub[name] = {k: r[k] for k in ("config", "steps", "us_per_step", "value", "layer_us", "sampler_us",
+                                       "sampler_draws", "roofline", "clocks") if k in r}
+        sub[name]["unit"] = "GB/s"
+        for k in ("self_attn_standalone", "long_output"):
+            if k in r:
+                sub[name][k] = r[k]
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -704,28 +810,26 @@ def main():
         cpu = {k: r[k] for k in ("value", "unit", "cores", "kind", "sample", "hardware_threads",
                                  "one_thread_workload1")}
 
-    assert int(ds.err.item()) == 0, "device error flag set during the timed steps"
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
-                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "bf16", "data": "synthetic",
-                "config": {**config, "l2": "inputs larger than L2 (%.1f GB per step vs 129 MB)" % (sb["step"] / 1e9)
-                           if sb["step"] > L2_BYTES else "inputs smaller than L2: warm-L2 figure"},
-                "us_per_step": ms * 1e3, "layer_us" if ds.fused else "self_attn_us": self_avg_ms * 1e3,
-                "sampler_us": samp_avg_ms * 1e3,
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "decoder_ends": {
-                    "lm_head": {"us": head_total_ms / K * 1e3, "batch": w.B, "K": 1024, "N": w.C * w.V,
-                                "weight_GBps": w.C * w.V * 1024 * 2 / (head_total_ms / K * 1e-3) / 1e9,
-                                "weights": f"{HEAD_COPIES} copies used in turn (more than L2)"},
-                    "embed": {"us": emb_total_ms / K * 1e3, "rows_gathered": w.B * w.C, "Dm": 1024,
-                              "tables": f"{HEAD_COPIES} copies used in turn (more than L2)"}},
-                "gpu_launches": ds.launches_per_step() * K, "launch_mode": mode,
-                "kernel_timing": "dominant kernel and sampler: K x layers (K) launches of the timed steps, "
-                                 "back to back in their own graph, events around it",
-                "clocks": clk.summary()}
-        if long_output is not None:
-            line["long_output"] = long_output
+        line = {"metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": ws, "steps": head["steps"],
+                "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": head["config"], "us_per_step": head["us_per_step"]}
+        for k in ("layer_us", "self_attn_us", "sampler_us", "sampler_draws", "roofline"):
+            if k in head:
+                line[k] = head[k]
+        line["cpu_baseline"] = cpu
+        line["e2e"] = head.get("e2e")
+        line["decoder_ends"] = head["decoder_ends"]
+        line["gpu_launches"] = head["gpu_launches"]
+        line["launch_mode"] = head["launch_mode"]
+        line["kernel_timing"] = ("dominant kernel and sampler: K x layers (K) launches of the timed steps, back to "
+                                 "back in their own graph, events around it")
+        line["clocks"] = head["clocks"]
+        if "long_output" in head:
+            line["long_output"] = head["long_output"]
+        if sub:
+            line["workloads"] = sub
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

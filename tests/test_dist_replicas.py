@@ -92,3 +92,26 @@ def test_reference_arm_under_torchrun_prints_once():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    # the same config object as the GPU arm prints for this workload, so that the two lines can be matched
+    sys.path.insert(0, root)
+    import bench
+    from decode_attention_self_gb300 import workloads as W
+
+    w = W.make_workload(1)
+    sb = bench.step_bytes(w)
+    assert d["config"] == bench.workload_config(w, sb, False, 2, bench.rotation_copies(sb["step"]))
+
+
+def test_batch1_steps_rotate_enough_copies_to_leave_l2():
+    # a step's data is used again only after >= 3x L2 of other data, or the figure says it is a warm-L2 one
+    import bench
+    from decode_attention_self_gb300 import workloads as W
+
+    n = {i: bench.rotation_copies(bench.step_bytes(W.make_workload(i))["step"]) for i in range(1, 6)}
+    assert n == {1: 1, 2: 3, 3: 2, 4: 1, 5: 1}
+    for i in (2, 3):
+        sb = bench.step_bytes(W.make_workload(i))["step"]
+        assert n[i] * sb >= 3 * bench.L2_BYTES > (n[i] - 1) * sb
+        assert "copies" in bench.l2_note(sb, n[i])
+    assert "warm-L2" in bench.l2_note(bench.step_bytes(W.make_workload(1))["step"], 1)
+    assert "larger than L2" in bench.l2_note(bench.step_bytes(W.make_workload(5))["step"], 1)
