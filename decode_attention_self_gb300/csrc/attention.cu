@@ -52,7 +52,8 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kD = kHeadDim;
 constexpr int kTile = kBlockKeys;
-constexpr int kMaxSplits = 8;   // CTAs per row: one portable cluster
+constexpr int kMaxSplits = 8;       // CTAs per row of the streaming variant: one portable cluster
+constexpr int kMaxSplitsWide = 16;  // of the pipelined variant: one non-portable cluster (small batch)
 
 struct SoftmaxPartial {
     float m;         // max of scaled log2-domain scores
@@ -435,7 +436,8 @@ template <typename KV, bool kPaged, bool kPipelined, bool kFused>
 __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kernel(const AttnParams p) {
     __shared__ float s_wm[kWarps], s_wl[kWarps];
     __shared__ float s_wacc[kWarps][kD];
-    __shared__ alignas(16) SoftmaxPartial s_parts[kMaxSplits];   // rank 0 of a cluster collects the CTAs' states
+    // rank 0 of a cluster collects the CTAs' states here
+    __shared__ alignas(16) SoftmaxPartial s_parts[kPipelined ? kMaxSplitsWide : kMaxSplits];
     __shared__ alignas(8) uint64_t s_parts_bar;   // streaming variant, rank 0: the other CTAs' states have landed
 
     const int h = blockIdx.y;
@@ -630,7 +632,12 @@ cudaError_t launch_variant(const AttnParams &p, int splits, cudaStream_t stream)
     unsigned zrows = (unsigned)p.B;
     if (kFused && p.xq) zrows += p.xpacked ? (unsigned)((p.B + splits - 1) / splits) : (unsigned)p.B;
     auto kern = decode_attn_kernel<KV, kPaged, kPipelined, kFused>;
-    if (splits < 1 || splits > kMaxSplits) return cudaErrorInvalidValue;   // rank 0 has kMaxSplits slots
+    // rank 0 has one state slot per CTA of its cluster
+    if (splits < 1 || splits > (kPipelined ? kMaxSplitsWide : kMaxSplits)) return cudaErrorInvalidValue;
+    if (splits > 8) {   // clusters of more than 8 CTAs are non-portable: allowed per kernel
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
     return launch_kernel(kern, dim3((unsigned)splits, (unsigned)p.H, zrows), dim3(kThreads), 0, stream,
                          (unsigned)splits, p);
 }
@@ -643,6 +650,7 @@ cudaError_t launch_layout(const AttnParams &p, bool paged, int splits, cudaStrea
     long long ctas = (long long)splits * p.H * p.B;
     if (kFused && p.xq) ctas += (long long)p.H * (p.xpacked ? p.B : (long long)splits * p.B);
     const bool pipelined = ctas <= (long long)kPipelinedCtasPerSm * current_device_sms();
+    if (!pipelined && splits > kMaxSplits) return cudaErrorInvalidValue;   // the plan keeps wide clusters resident
     if (paged)
         return pipelined ? launch_variant<KV, true, true, kFused>(p, splits, stream)
                          : launch_variant<KV, true, false, kFused>(p, splits, stream);

@@ -143,10 +143,15 @@ int dr_plan_splits(int B, int H, int max_len, int kv_dtype, int num_sms) {
     // ...and at least kFillCtasPerSm CTAs per SM when the rows alone are fewer...
     const long long fill = (kFillCtasPerSm * num_sms + rows - 1) / rows;
     if (fill > s) s = fill;
-    // ...but never fewer than 4 tiles (64 keys) per CTA, nor more than one cluster.
+    // ...but never fewer than 4 tiles (64 keys) per CTA, nor more than one portable cluster...
     const long long by_tiles = (tiles + 3) / 4;
     if (s > by_tiles) s = by_tiles;
     if (s > dr::max_cluster_size()) s = dr::max_cluster_size();
+    // ...except for a few long rows (small batch): when 16 CTAs per row still leave room for the next launch's
+    // grid (at most 2 CTAs per SM) and 8 CTAs would each stream 16 tiles or more, one non-portable cluster of
+    // 16 halves every CTA's chain of dependent tiles (batch 1, 2048 + 64 keys: 4.87 -> 4.53 us per layer;
+    // with 8 tiles per CTA, or more CTAs per SM, 16-CTA clusters were slower).
+    if (s == dr::max_cluster_size() && rows * 16 <= 2LL * num_sms && tiles >= 16LL * 8) s = 16;
     return s < 1 ? 1 : (int)s;
 }
 

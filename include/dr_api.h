@@ -322,7 +322,9 @@ dr_status dr_lm_head_stall_test(const void *hidden, const void *W, int B, int K,
  * DR_KV_BF16) on a GPU with num_sms SMs.  Each CTA of the cluster takes an
  * equal run of whole 16-key blocks of the row.  The plan: at most 256 KiB
  * of K+V per CTA at the longest row, at least 6 CTAs per SM when the rows
- * alone are fewer, at least 64 keys per CTA, at most 8 CTAs.  Pure
+ * alone are fewer, at least 64 keys per CTA, at most 8 CTAs -- or 16 (a
+ * non-portable cluster) when 8 would each take at least 256 keys and 16 per
+ * row come to at most 2 CTAs per SM (a few long rows: batch 1).  Pure
  * arithmetic; touches no device.  Returns 1 for non-positive sizes or an
  * unknown kv_dtype.
  */

@@ -147,6 +147,14 @@ def test_split_plan(lib):
     assert plan(1, 16, 1024, BF16, 152) == 8      # batch 1: fill the GPU, capped by the cluster size
     assert plan(1, 16, 64, BF16, 152) == 1        # a 64-key row is one CTA
     assert plan(1, 16, 200, BF16, 152) == 4       # 13 tiles, at least 4 per CTA: ceil(13 / 4) = 4 CTAs
+    # a few long rows: 16 CTAs per row (a non-portable cluster) when 8 would take >= 16 tiles each and
+    # 16 per row is at most 2 CTAs per SM
+    assert plan(1, 16, 2048, BF16, 152) == 16
+    assert plan(1, 16, 4096, E4M3, 152) == 16
+    assert plan(1, 19, 2048, BF16, 152) == 16     # 304 CTAs on 152 SMs
+    assert plan(1, 20, 2048, BF16, 152) == 8      # 320: more than 2 per SM
+    assert plan(1, 16, 2000, BF16, 152) == 8      # 125 tiles: fewer than 16 per CTA at 8 CTAs
+    assert plan(2, 16, 4096, BF16, 152) == 8
     assert plan(128, 16, 4096, 7, 152) == 1       # unknown storage type
     assert plan(0, 16, 4096, BF16, 152) == 1
 

@@ -337,21 +337,69 @@ def test_calls_capture_into_a_cuda_graph(api, cuda_device):
 def test_row_result_independent_of_batch_and_kernel_variant(api, cuda_device):
     # A row alone (B=1: the whole grid is resident, the pipelined variant runs) and the same row inside a
     # batch of 8 (1024 CTAs, more than 4 per SM: the streaming variant runs) share the split plan (8 CTAs
-    # per row for a 4096-key bound), and the two variants do the same arithmetic in the same order: the
+    # per row for a 2000-key bound), and the two variants do the same arithmetic in the same order: the
     # outputs must be bit-identical.
     from decode_attention_self_gb300 import api as _api
     dev = cuda_device
-    lens = [4000] + [int(x) for x in np.random.default_rng(13).integers(1000, 4096, size=7)]
-    w, cache, q = ragged_case("paged", lens, 4096, seed=13)
+    lens = [2000] + [int(x) for x in np.random.default_rng(13).integers(1000, 2000, size=7)]
+    w, cache, q = ragged_case("paged", lens, 2048, seed=13)
     bf16 = api.DR_KV_BF16
-    assert api.dr_plan_splits(1, 16, 4096, bf16, 152) == api.dr_plan_splits(8, 16, 4096, bf16, 152) == 8
+    assert api.dr_plan_splits(1, 16, 2000, bf16, 152) == api.dr_plan_splits(8, 16, 2000, bf16, 152) == 8
     kv = to_dev(cache, dev)
     seq = torch.from_numpy(w.seq_len).to(dev)
     big = torch.empty((w.B, 16, D), dtype=torch.float32, device=dev)
-    api.dr_decode_self_attn(q.to(dev), kv, seq, big, max_seq_len_hint=4096)
+    api.dr_decode_self_attn(q.to(dev), kv, seq, big, max_seq_len_hint=2000)
     one_kv = _api.KVCache(kv.k, kv.v, kv.block_table[:1].contiguous())
     one = torch.empty((1, 16, D), dtype=torch.float32, device=dev)
-    api.dr_decode_self_attn(q[:1].contiguous().to(dev), one_kv, seq[:1].contiguous(), one, max_seq_len_hint=4096)
+    api.dr_decode_self_attn(q[:1].contiguous().to(dev), one_kv, seq[:1].contiguous(), one, max_seq_len_hint=2000)
     torch.cuda.synchronize()
     assert torch.equal(one[0], big[0])
     assert_attn_close(big[:2], oracle_self(w, cache, q, default_scale(D))[:2])
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+@pytest.mark.parametrize("L", [2047, 2048, 3001, 4096])
+def test_wide_clusters_for_few_long_rows(api, cuda_device, layout, L):
+    # Batch 1 with rows of 2048 keys or more: 16 CTAs per row, one non-portable cluster, 16 state slots in
+    # rank 0.  Rows shorter than the bound leave the last CTAs of their cluster without a tile.
+    bf16 = api.DR_KV_BF16
+    assert api.dr_plan_splits(1, 16, L, bf16, 152) == 16
+    dev = cuda_device
+    w, cache, q = ragged_case(layout, [L], 4096, seed=40 + L % 7)
+    kv = to_dev(cache, dev)
+    seq = torch.from_numpy(w.seq_len).to(dev)
+    out = torch.empty((1, 16, D), dtype=torch.float32, device=dev)
+    for hint in (L, 4096):
+        api.dr_decode_self_attn(q.to(dev), kv, seq, out, max_seq_len_hint=hint)
+        assert_attn_close(out, oracle_self(w, cache, q, default_scale(D)), f"{layout} L={L} hint {hint}")
+    # and the same row as a description row (dr_decode_cross_attn plans its rows the same way)
+    xk, xv = cache.k, cache.v
+    if layout == "contiguous":
+        api.dr_decode_cross_attn(q.to(dev), xk.to(dev), xv.to(dev), seq, out)
+        assert_attn_close(out, oracle_self(w, cache, q, default_scale(D)), f"cross L={L}")
+
+
+def test_wide_clusters_paged_equals_contiguous_bitwise(api, cuda_device):
+    # the 16-CTA split partitions the row by tiles exactly as the 8-CTA one does: the paged layout with a
+    # shuffled table reproduces the contiguous result bit for bit
+    dev = cuda_device
+    lens = [3001]
+    wc, cc, q = ragged_case("contiguous", lens, 4096, seed=6)
+    wp = W.Workload(106, "edge", 1, 1, "paged", wc.seq_len, 4096, wc.seq_len, 4096, 1.0, 1, 1.0, wc.seeds, wc.steps)
+    table, NB = W.make_block_table(wp, "cpu", 6)
+    kp = torch.full((NB, 16, 16, D), float("nan"), dtype=torch.bfloat16)
+    vp = kp.clone()
+    for j in range((lens[0] + 15) // 16):
+        kp[table[0, j]] = cc.k[0, :, 16 * j:16 * j + 16]
+        vp[table[0, j]] = cc.v[0, :, 16 * j:16 * j + 16]
+    from decode_attention_self_gb300 import api as _api
+    kvc = _api.KVCache(cc.k.to(dev), cc.v.to(dev))
+    kvp = _api.KVCache(kp.to(dev), vp.to(dev), table.to(dev))
+    seq = torch.from_numpy(wc.seq_len).to(dev)
+    oc = torch.empty((1, 16, D), dtype=torch.float32, device=dev)
+    op = torch.empty_like(oc)
+    assert api.dr_plan_splits(1, 16, 4096, api.DR_KV_BF16, 152) == 16
+    api.dr_decode_self_attn(q.to(dev), kvc, seq, oc, max_seq_len_hint=4096)
+    api.dr_decode_self_attn(q.to(dev), kvp, seq, op, max_seq_len_hint=4096)
+    torch.cuda.synchronize()
+    assert torch.equal(oc, op)

@@ -184,3 +184,17 @@ def test_fp8_fused_layer_edge_lengths(api, cuda_device, layout):
         assert np.array_equal(codes(kv.k), kh) and np.array_equal(codes(kv.v), vh), f"codes, hint {hint}"
         assert_attn_close(out, ref, f"fp8 fused self {layout} hint {hint}")
         assert_attn_close(outx, refx, f"fused cross {layout} hint {hint}")
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+def test_fp8_wide_clusters_for_few_long_rows(api, cuda_device, layout):
+    # batch 1, e4m3 rows of 2048 keys or more: one non-portable cluster of 16 CTAs per row
+    assert api.dr_plan_splits(1, 16, 4096, api.DR_KV_FP8_E4M3, 152) == 16
+    dev = cuda_device
+    lens = [3500]
+    w, c = ragged(layout, lens, 4096, 77, filled=np.array(lens, np.int32))
+    q = W.randn_bf16((1, 16, D), "cpu", 304, 1)
+    out = torch.empty((1, 16, D), dtype=torch.float32, device=dev)
+    api.dr_decode_self_attn(q.to(dev), dev_cache(api, c, dev), torch.from_numpy(w.seq_len).to(dev), out,
+                            max_seq_len_hint=4096)
+    assert_attn_close(out, oracle_fp8(w, c, q), f"fp8 {layout} 16 CTAs per row")
