@@ -668,9 +668,11 @@ def measure(w: W.Workload, K: int, warmup: int, dev, rank: int, ws: int, dist, *
     if "self_attn" in t_ms:
         sa_ms = t_ms["self_attn"] / (K * w.layers)
         sa = sb["self"] / (sa_ms * 1e-3) / 1e9
+        sa_traffic = committed_traffic(f"decode_attn_kernel workload {w.index} {'e4m3' if fp8 else 'bf16'}")
         r["self_attn_standalone"] = {"us": sa_ms * 1e3, "achieved": sa, "frac": sa / peaks["hbm_gbs"],
                                      "frac_of_nominal_8tbs": sa / NOMINAL_HBM_GBS,
                                      "algorithmic_bytes_per_launch": sb["self"],
+                                     "traffic": sa_traffic["dram_bytes_per_launch"] if sa_traffic else None,
                                      "kernel": "decode_attn_kernel (dr_decode_self_attn)"}
     if decoder_ends:
         r["decoder_ends"] = {
