@@ -49,12 +49,15 @@ _lib.dr_sample_topk_delayed.argtypes = [_vp, _i, _i, _i, _i, _f, _i, _vp, _vp, c
 _lib.dr_embed_tokens.argtypes = [_vp, _vp, _i, _i, _i, _i, _vp, _i, _vp, _vp]
 _lib.dr_lm_head.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp]
 _lib.dr_lm_head_stall_test.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _i, _vp]
+_lib.dr_decode_self_attn_stall_test.argtypes = [_vp, ctypes.POINTER(dr_kv_cache), _vp, _i, _i, _i, _i, _f, _vp, _i, _vp,
+                                                _i, _vp]
 _lib.dr_plan_splits.argtypes = [_i, _i, _i, _i, _i]
 _lib.dr_plan_splits.restype = _i
 _lib.dr_status_string.argtypes = [_i]
 _lib.dr_status_string.restype = ctypes.c_char_p
 for _fn in ("dr_kv_append", "dr_decode_self_attn", "dr_decode_cross_attn", "dr_decode_layer",
-            "dr_sample_topk_delayed", "dr_embed_tokens", "dr_lm_head", "dr_lm_head_stall_test"):
+            "dr_sample_topk_delayed", "dr_embed_tokens", "dr_lm_head", "dr_lm_head_stall_test",
+            "dr_decode_self_attn_stall_test"):
     getattr(_lib, _fn).restype = _i
 
 
@@ -161,6 +164,22 @@ def dr_decode_self_attn(q: torch.Tensor, cache: KVCache, seq_len: torch.Tensor, 
            _lib.dr_decode_self_attn(_ptr(q, torch.bfloat16, "q"), ctypes.byref(c), _ptr(seq_len, torch.int32, "seq_len"),
                                     B, H, D, int(max_seq_len_hint), float(scale), _ptr(out, None, "out"), od,
                                     _ptr(err_flag, torch.int32, "err_flag"), _stream(stream)))
+    return out
+
+
+def dr_decode_self_attn_stall_test(q: torch.Tensor, cache: KVCache, seq_len: torch.Tensor, out: torch.Tensor,
+                                   stall_row: int, max_seq_len_hint: int = 0, scale: float = 0.0,
+                                   err_flag: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Test hook: dr_decode_self_attn with row stall_row's cluster merge left waiting until its bound runs out."""
+    B, H, D = q.shape
+    c = cache.as_c()
+    od = DR_F32 if out.dtype == torch.float32 else DR_BF16
+    _check("dr_decode_self_attn_stall_test",
+           _lib.dr_decode_self_attn_stall_test(_ptr(q, torch.bfloat16, "q"), ctypes.byref(c),
+                                               _ptr(seq_len, torch.int32, "seq_len"), B, H, D, int(max_seq_len_hint),
+                                               float(scale), _ptr(out, None, "out"), od,
+                                               _ptr(err_flag, torch.int32, "err_flag"), int(stall_row),
+                                               _stream(stream)))
     return out
 
 

@@ -567,6 +567,7 @@ __global__ void __launch_bounds__(kThreads, kPipelined ? 4 : 8) decode_attn_kern
         // waits for those bytes and merges, its own state first.  The CTAs that finish early free their SM
         // at once (batch 32: fused layer 35.7 -> 34.8 us; batch 128: 187.3 -> 186.0 us).
         if (split != 0) {
+            if (split == 1 && (long long)row == p.stall_row) return;   // test hook: this state never arrives
             if (d < kD) {
                 const uint32_t bar = map_rank0(smem_addr(&s_parts_bar));
                 SoftmaxPartial *slot = &s_parts[split];

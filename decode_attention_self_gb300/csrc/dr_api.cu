@@ -197,6 +197,28 @@ dr_status dr_decode_self_attn(const void *q, const dr_kv_cache *cache, const int
     return launch(p, cache->layout == DR_KV_PAGED, max_seq_len_hint, stream);
 }
 
+dr_status dr_decode_self_attn_stall_test(const void *q, const dr_kv_cache *cache, const int32_t *seq_len, int B, int H,
+                                        int D, int max_seq_len_hint, float scale, void *out, dr_dtype out_dtype,
+                                        int32_t *err_flag, int stall_row, void *stream) {
+    if (B < 1 || H < 1 || stall_row < 0 || (long long)stall_row >= (long long)B * H) return DR_ERR_INVALID_ARG;
+    dr_status st = check_dims(B, H, D);
+    if (st != DR_OK) return st;
+    int cap = 0;
+    st = check_cache(cache, &cap);
+    if (st != DR_OK) return st;
+    st = check_attn_args(q, seq_len, out, out_dtype, scale);
+    if (st != DR_OK) return st;
+    dr::AttnParams p;
+    fill_cache(p, q, cache, seq_len, B, H, cap, scale, out, out_dtype, err_flag);
+    p.stall_row = stall_row;
+    const int sms = dr::current_device_sms();
+    if (sms <= 0) return DR_ERR_CUDA;
+    // only the streaming variant (a grid larger than 4 CTAs per SM) with split rows waits on an mbarrier
+    const int splits = self_splits(p, max_seq_len_hint, sms);
+    if (splits < 2 || (long long)splits * H * B <= 4LL * sms) return DR_ERR_UNSUPPORTED;
+    return from_cuda(dr::launch_decode_attn(p, cache->layout == DR_KV_PAGED, splits, static_cast<cudaStream_t>(stream)));
+}
+
 dr_status dr_decode_cross_attn(const void *q, const void *k_enc, const void *v_enc, const int32_t *enc_len, int B,
                                int H, int D, int Lc_max, float scale, void *out, dr_dtype out_dtype,
                                int32_t *err_flag, void *stream) {

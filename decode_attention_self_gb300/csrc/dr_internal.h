@@ -82,6 +82,9 @@ struct AttnParams {
     float xqscale;           // softmax scale * log2(e) for the cross rows
     void *xout;              // [B][H][64]
     int32_t xpacked;         // 1: one CTA per cross row, gridDim.x rows per cluster; 0: rows split like self rows
+    // Test hook (streaming variant only): CTA 1 of row b*H + h == stall_row never sends its state, so rank 0's
+    // bounded wait for it runs out; -1 (every ordinary call): none.
+    int32_t stall_row = -1;
 };
 
 cudaError_t launch_decode_attn(const AttnParams &p, bool paged, int splits, cudaStream_t stream);

@@ -315,6 +315,25 @@ dr_status dr_lm_head_stall_test(const void *hidden, const void *W, int B, int K,
                                 int32_t *err_flag, int stall_slab, void *stream);
 
 /*
+ * dr_decode_self_attn_stall_test -- TEST HOOK, never needed in use.  The
+ * same call as dr_decode_self_attn, except that CTA 1 of row
+ * stall_row = b*H + h never sends its softmax state to the row's CTA rank 0.
+ * That CTA's bounded wait for the state then runs out (after about 2 s):
+ * DR_ERRF_TIMEOUT is ORed into *err_flag, that row's output is left
+ * unwritten, and every other row is written as by dr_decode_self_attn.
+ * Nothing faults or hangs, and later calls on the same context work
+ * normally.  The tests use it to check the failure path of the cluster
+ * merge's wait; the paper has no counterpart.
+ *   0 <= stall_row < B*H (DR_ERR_INVALID_ARG otherwise).  The call must run
+ *   the kernel variant whose split rows merge through that wait: at least 2
+ *   CTAs per row (dr_plan_splits) and more than 4 CTAs per SM in all
+ *   (DR_ERR_UNSUPPORTED otherwise).  The rest as dr_decode_self_attn.
+ */
+dr_status dr_decode_self_attn_stall_test(const void *q, const dr_kv_cache *cache, const int32_t *seq_len, int B, int H,
+                                        int D, int max_seq_len_hint, float scale, void *out, dr_dtype out_dtype,
+                                        int32_t *err_flag, int stall_row, void *stream);
+
+/*
  * dr_plan_splits -- host-only query: how many CTAs (one thread-block
  * cluster) share each (b, h) row of an attention call with this batch,
  * head count, length bound and KV storage type (DR_KV_BF16 or

@@ -135,6 +135,17 @@ def test_embedding_validation(lib):
     assert call(table=FAKE + 8) == 1              # table must be 16-byte aligned
 
 
+def test_self_attn_stall_hook_validation(lib):
+    # the row must exist; the check comes before anything needs a device
+    c = Cache(0, 2048, 0, 0, 0, 0, FAKE, FAKE, None)
+    vp = ctypes.c_void_p
+    call = lambda row, B=2: lib.dr_decode_self_attn_stall_test(vp(FAKE), ctypes.byref(c), vp(FAKE), B, 16, 64, 0,
+                                                               ctypes.c_float(0), vp(FAKE), 0, None, row, None)
+    assert call(-1) == 1
+    assert call(32) == 1
+    assert call(0, B=0) == 1
+
+
 def test_split_plan(lib):
     # split count per (b, h) row: one cluster of at most 8 CTAs, >= 64 keys each, <= 256 KiB of K+V each at
     # the longest row, and at least 6 CTAs per SM of a 152-SM GPU when the rows alone are fewer.

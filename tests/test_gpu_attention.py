@@ -403,3 +403,32 @@ def test_wide_clusters_paged_equals_contiguous_bitwise(api, cuda_device):
     api.dr_decode_self_attn(q.to(dev), kvp, seq, op, max_seq_len_hint=4096)
     torch.cuda.synchronize()
     assert torch.equal(oc, op)
+
+
+def test_cluster_merge_wait_that_runs_out(api, cuda_device):
+    # Test hook: CTA 1 of row 5 (b=0, h=5) never sends its state to the row's rank 0, whose bounded wait for it
+    # gives up after about 2 s.  DR_ERRF_TIMEOUT is set, that row's output stays unwritten, every other row is
+    # right, and the next ordinary call on the same context is right everywhere.  Batch 32 of 2048 keys:
+    # 2 CTAs per row, 1024 CTAs, the streaming variant whose split rows merge through that wait.
+    dev = cuda_device
+    lens = [2048] * 32
+    w, cache, q = ragged_case("paged", lens, 2048, seed=31)
+    assert api.dr_plan_splits(32, 16, 2048, api.DR_KV_BF16, 152) == 2
+    kv = to_dev(cache, dev)
+    seq = torch.from_numpy(w.seq_len).to(dev)
+    ref = oracle_self(w, cache, q, default_scale(D))
+    out = torch.full((w.B, 16, D), float("nan"), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    api.dr_decode_self_attn_stall_test(q.to(dev), kv, seq, out, 5, max_seq_len_hint=2048, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & api.DR_ERRF_TIMEOUT
+    got = out.cpu().numpy()
+    assert np.isnan(got[0, 5]).all()
+    keep = np.ones((w.B, 16), bool)
+    keep[0, 5] = False
+    assert (np.abs(got[keep] - ref[keep]) <= 2e-3).all()
+    err.zero_()
+    api.dr_decode_self_attn(q.to(dev), kv, seq, out, max_seq_len_hint=2048, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attn_close(out, ref, "after the wait that ran out")
