@@ -168,3 +168,49 @@ def test_fused_layer_cross_row_layouts(api, cuda_device, B, self_len, enc_max):
                       f"self (splits {s_self})")
     assert_attn_close(outx, oracle.attn_contiguous(W.bits(qx), W.bits(kx), W.bits(vx), enc_len, default_scale(D)),
                       f"cross (standalone plan {s_cross}, self plan {s_self})")
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+@pytest.mark.parametrize("L,enc_max", [(2048, 64), (2050, 3000), (4096, 700)])
+def test_fused_layer_wide_clusters(api, cuda_device, layout, L, enc_max):
+    # Batch 1 with a self row of 2048 keys or more: 16 CTAs per row in one non-portable cluster; the description
+    # rows are either packed 16 to a cluster (64 keys) or split 16 ways like the self rows (3000 keys).  The
+    # appended key opens a new tile (2050) or fills the cache's last slot (4096).  The fused launch equals the
+    # separate calls bit for bit (cache and self-attention) and the oracle within tolerance.
+    dev = cuda_device
+    assert api.dr_plan_splits(1, 16, L, api.DR_KV_BF16, 152) == 16
+    lens = np.array([L], np.int32)
+    enc_len = np.array([enc_max - 7], np.int32)
+    w = W.Workload(121, "wide", 1, 1, layout, lens, 4096, enc_len, enc_max, 1.0, 1, 1.0, np.zeros(1, np.uint64),
+                   np.zeros(1, np.int32))
+    cache = W.make_self_cache(w, L % 97)
+    q, qx, kn, vn = W.make_step_inputs(w, 1)
+    kx, vx = W.make_cross_kv(w, 1)
+    seq, enc = torch.from_numpy(lens).to(dev), torch.from_numpy(enc_len).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kv_f, kv_s = dev_cache(api, cache, dev), dev_cache(api, cache, dev)
+    out_f = torch.empty((1, 16, D), dtype=torch.float32, device=dev)
+    outx_f, out_s, outx_s = torch.empty_like(out_f), torch.empty_like(out_f), torch.empty_like(out_f)
+    qd, qxd, knd, vnd, kxd, vxd = (t.to(dev) for t in (q, qx, kn, vn, kx, vx))
+    api.dr_decode_layer(qd, kv_f, knd, vnd, seq, qxd, kxd, vxd, enc, out_f, outx_f, max_seq_len_hint=L, err_flag=err)
+    api.dr_kv_append(kv_s, knd, vnd, seq - 1, err_flag=err)
+    api.dr_decode_self_attn(qd, kv_s, seq, out_s, max_seq_len_hint=L, err_flag=err)
+    api.dr_decode_cross_attn(qxd, kxd, vxd, enc, outx_s, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    # bit patterns: the slots past the valid keys hold NaN
+    assert np.array_equal(W.bits(kv_f.k), W.bits(kv_s.k)) and np.array_equal(W.bits(kv_f.v), W.bits(kv_s.v))
+    assert torch.equal(out_f, out_s)
+    kh, vh = W.bits(cache.k).copy(), W.bits(cache.v).copy()
+    if layout == "contiguous":
+        oracle.kv_append_contiguous(kh, vh, W.bits(kn), W.bits(vn), lens - 1)
+        ref = oracle.attn_contiguous(W.bits(q), kh, vh, lens, default_scale(D))
+    else:
+        t = cache.block_table.numpy()
+        oracle.kv_append_paged(kh, vh, t, W.bits(kn), W.bits(vn), lens - 1)
+        ref = oracle.attn_paged(W.bits(q), kh, vh, t, lens, default_scale(D))
+    assert np.array_equal(W.bits(kv_f.k), kh) and np.array_equal(W.bits(kv_f.v), vh)
+    assert_attn_close(out_f, ref, f"self, {layout} L={L}")
+    refx = oracle.attn_contiguous(W.bits(qx), W.bits(kx), W.bits(vx), enc_len, default_scale(D))
+    assert_attn_close(outx_f, refx, f"cross, {layout} L={L}")
+    assert_attn_close(outx_s, refx, f"standalone cross, {layout} L={L}")
