@@ -119,6 +119,15 @@ __global__ void __launch_bounds__(kThreads, kThreads == kNarrowThreads ? 8 : kWi
     const int b = blockIdx.y;
     const int t = threadIdx.x;
     const int lane = t & 31, warp = t >> 5;
+    // The row's logits are loaded before the step is known, so that the two loads are in flight together (a
+    // padded codebook does not use them; the row exists either way).
+    const float *row = p.logits + ((size_t)b * p.C + c) * (size_t)p.ldv;
+    float lg[EPT];
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+        const int i = t + kThreads * j;
+        lg[j] = i < p.V ? __ldg(row + i) : 0.f;
+    }
     const int step = p.step[b];
     const bool active = step > c;   // delay pattern: codebook c is padded while step <= c
     float *prow = p.probs ? p.probs + ((size_t)b * p.C + c) * (size_t)p.V : nullptr;
@@ -128,7 +137,6 @@ __global__ void __launch_bounds__(kThreads, kThreads == kNarrowThreads ? 8 : kWi
         if (prow)
             for (int i = t; i < p.V; i += kThreads) prow[i] = 0.f;
     } else {
-        const float *row = p.logits + ((size_t)b * p.C + c) * (size_t)p.ldv;
         // Only the order keys stay in registers; key_value() inverts the map.
         uint32_t key[EPT];
         uint32_t valid = 0;
@@ -137,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, kThreads == kNarrowThreads ? 8 : kWi
             const int i = t + kThreads * j;
             key[j] = 0u;
             if (i < p.V) {
-                key[j] = order_key(__fdiv_rn(__ldg(row + i), p.temperature));
+                key[j] = order_key(__fdiv_rn(lg[j], p.temperature));
                 valid |= 1u << j;
             }
         }
