@@ -6,8 +6,10 @@ every layer, then the fused sampler, on one batch of synthetic input.
 Default workload: 5, the batch-128 stress case (24 layers, paged bf16 KV with
 block size 16, self lengths U{512..4096}, cross 256, sampler 128x9x1088 with
 planted ties, top-k 250, T=0.7, per-row seeds) -- the batch >= 32 regime in
-which the self-attention's HBM bandwidth is the figure of merit.  Workloads
-1-4 are available with --workload.
+which the self-attention's HBM bandwidth is the figure of merit.  After it the
+default run measures workloads 1-4 and the e4m3 cache at 4 and 5 (--sub), and
+reports them in the line's "workloads" object, each with its own clock record;
+--workload I --sub none measures one workload alone.
 
 Metric: algorithmic HBM GB/s of the whole decode step (bytes the step must
 move: valid K/V, q, outputs, block-table entries, appended rows, logits and
