@@ -384,7 +384,9 @@ class HostStep:
     one pinned host buffer and move in one copy.  Inputs and drawn tokens are double-buffered on the device,
     as a serving loop would do it: while step i runs on the compute stream, a copy stream reads back step
     i - 1's tokens and brings step i + 1's inputs into the other buffer set (the one step i - 1 used, once
-    that step has finished).  Every copy and every token read-back is inside the timed region."""
+    that step has finished).  Every copy and every token read-back is inside the timed region.  When the step
+    rotates copies of the layers' buffers (batch 1), every copy reads the same staged inputs; only the caches
+    and the description K/V rotate."""
 
     KEYS = ("q", "qx", "kn", "vn")
 
@@ -412,21 +414,23 @@ class HostStep:
         self.h2d = sum(t.numel() * t.element_size() for _, t in srcs)
         self.d2h = self.h_tokens.numel() * 4
         self.copy_stream = torch.cuda.Stream()
-        self._orig = ({l: {k: L[k] for k in self.KEYS} for l, L in enumerate(ds.layers)}, ds.logits, ds.pos, ds.seq,
-                      ds.tokens)
+        self._orig = ([{l: {k: L[k] for k in self.KEYS} for l, L in enumerate(layers)} for layers in ds.sets],
+                      ds.logits, ds.pos, ds.seq, ds.tokens)
 
     def _use(self, st):
         ds, views = self.ds, st["views"]
-        for l, L in enumerate(ds.layers):
-            for k in self.KEYS:
-                L[k] = views[("layer", l, k)]
+        for layers in ds.sets:
+            for l, L in enumerate(layers):
+                for k in self.KEYS:
+                    L[k] = views[("layer", l, k)]
         ds.logits, ds.pos, ds.seq, ds.tokens = views[("logits",)], views[("pos",)], views[("seq",)], st["tokens"]
 
     def _restore(self):
         ds = self.ds
-        layers, ds.logits, ds.pos, ds.seq, ds.tokens = self._orig
-        for l, L in enumerate(ds.layers):
-            L.update(layers[l])
+        sets, ds.logits, ds.pos, ds.seq, ds.tokens = self._orig
+        for layers, saved in zip(ds.sets, sets):
+            for l, L in enumerate(layers):
+                L.update(saved[l])
 
     def run_steps(self, K: int):
         """K steps: compute on the current stream, input copies on the copy stream, ordered by events."""
@@ -441,7 +445,7 @@ class HostStep:
         for i in range(K):
             main.wait_event(copied[i])
             self._use(self.sets[i % 2])
-            self.ds.run()
+            self.ds.run(i)
             done[i].record(main)
             with torch.cuda.stream(side):
                 side.wait_event(done[i])              # step i has drawn its tokens and read its inputs
@@ -800,9 +804,10 @@ def main():
         sw = W.make_workload(idx)
         scopies = rotation_copies(step_bytes(sw, kv_bytes=1 if sfp8 else 2)["step"])
         r = measure(sw, args.steps, args.warmup, dev, rank, ws, dist, fp8=sfp8, copies=scopies, eager=args.eager,
-                    standalone_self=idx == 4, long_output=idx == 3, gpu_index=local)
+                    standalone_self=idx == 4, long_output=idx == 3, e2e=name == "2" and not args.no_e2e,
+                    gpu_index=local)
         sub[name] = {k: r[k] for k in ("config", "steps", "us_per_step", "value", "layer_us", "sampler_us",
-                                       "sampler_draws", "roofline", "clocks") if k in r}
+                                       "sampler_draws", "roofline", "clocks", "e2e") if k in r}
         sub[name]["unit"] = "GB/s"
         for k in ("self_attn_standalone", "long_output"):
             if k in r:
