@@ -286,3 +286,28 @@ def test_nan_logits_token_stays_in_range(api, cuda_device, k):
                         1024, want_probs=False)
     t = tok.cpu().numpy()
     assert ((t >= 0) & (t < V)).all(), t
+
+
+@pytest.mark.parametrize("k", [1, 13, 50, 64, 70])
+def test_order_keys_across_every_float_class(api, cuda_device, k):
+    # The radix select orders the logits through a float -> uint32 key map.  Here 64 entries of each row lie in
+    # [0.5, 30] and the rest are random bit patterns of every other class -- negative values of every exponent,
+    # -inf, subnormals of both signs, +-0 and tiny positives -- so the first radix pass sees keys in every bin.
+    # The top 64 are the band; k = 70 takes six more from the background's largest, which are planted tiny
+    # non-negative values (zeros and subnormals, so also ties), and stay within fp32's exp range of the maximum.
+    rng = np.random.default_rng(90 + k)
+    B, C, V = 4, 9, 1088
+    bits = rng.integers(0, 2 ** 32, size=(B, C, V), dtype=np.uint64).astype(np.uint32)
+    bg = bits.view(np.float32).copy()
+    bad = ~np.isfinite(bg) | (bg > 1e-30)
+    bg[bad] = -np.abs(np.where(np.isnan(bg[bad]), 1.0, bg[bad]))        # background: every float <= 1e-30
+    x = bg
+    for b in range(B):
+        for c in range(C):
+            pos = rng.choice(V, size=64 + 10 + 3, replace=False)
+            x[b, c, pos[:64]] = rng.uniform(0.5, 30.0, size=64).astype(np.float32)
+            x[b, c, pos[64:74]] = np.array([0.0, -0.0, 0.0, 1e-45, 3e-39, 1e-38, 1e-40, -0.0, 0.0, 2e-45],
+                                           np.float32)
+            x[b, c, pos[74:]] = -np.inf
+    assert np.isfinite(x[x > 0]).all() and not np.isnan(x).any()
+    check(api, cuda_device, x, 1.0, k, np.arange(B, dtype=np.uint64) + 3, np.full(B, 20, np.int32), 5)
