@@ -805,9 +805,9 @@ def main():
         scopies = rotation_copies(step_bytes(sw, kv_bytes=1 if sfp8 else 2)["step"])
         r = measure(sw, args.steps, args.warmup, dev, rank, ws, dist, fp8=sfp8, copies=scopies, eager=args.eager,
                     standalone_self=idx == 4, long_output=idx == 3, e2e=name == "2" and not args.no_e2e,
-                    gpu_index=local)
+                    decoder_ends=name == "2", gpu_index=local)
         sub[name] = {k: r[k] for k in ("config", "steps", "us_per_step", "value", "layer_us", "sampler_us",
-                                       "sampler_draws", "roofline", "clocks", "e2e") if k in r}
+                                       "sampler_draws", "roofline", "clocks", "e2e", "decoder_ends") if k in r}
         sub[name]["unit"] = "GB/s"
         for k in ("self_attn_standalone", "long_output"):
             if k in r:
