@@ -334,6 +334,42 @@ def test_calls_capture_into_a_cuda_graph(api, cuda_device):
     assert torch.equal(out_e, out_g)
 
 
+def test_two_streams_at_once_give_the_single_stream_bits(api, cuda_device):
+    # The library holds no state between calls, so two problems launched on two streams, interleaved and free
+    # to run at the same time, give the bits each gives alone.  One problem is small (its whole grid is
+    # resident: the pipelined variant, clusters of 8), the other large (2 CTAs per row, 1280 CTAs: the
+    # streaming variant, whose split rows merge on an mbarrier).
+    dev = cuda_device
+    rng = np.random.default_rng(41)
+    small = ragged_case("paged", [1500, 300], 2048, seed=41)
+    large = ragged_case("contiguous", [int(x) for x in rng.integers(256, 1024, size=40)], 1024, seed=42)
+    bf16 = api.DR_KV_BF16
+    assert api.dr_plan_splits(2, 16, 2048, bf16, 152) == 8 and api.dr_plan_splits(40, 16, 1024, bf16, 152) == 2
+    cases = []
+    for w, cache, q in (small, large):
+        cases.append((w, cache, q, q.to(dev), to_dev(cache, dev), torch.from_numpy(w.seq_len).to(dev)))
+    alone = []
+    for w, _, _, qd, kv, seq in cases:
+        o = torch.empty((w.B, 16, D), dtype=torch.float32, device=dev)
+        api.dr_decode_self_attn(qd, kv, seq, o)
+        alone.append(o)
+    torch.cuda.synchronize()
+    reps = 6
+    outs = [[torch.empty_like(o) for _ in range(reps)] for o in alone]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for it in range(reps):
+        for i, (_, _, _, qd, kv, seq) in enumerate(cases):
+            api.dr_decode_self_attn(qd, kv, seq, outs[i][it], stream=streams[i])
+    torch.cuda.synchronize()
+    for i in range(2):
+        for it in range(reps):
+            assert torch.equal(outs[i][it], alone[i]), (i, it)
+    for (w, cache, q, *_), o in zip(cases, alone):
+        assert_attn_close(o, oracle_self(w, cache, q, default_scale(D)))
+
+
 def test_row_result_independent_of_batch_and_kernel_variant(api, cuda_device):
     # A row alone (B=1: the whole grid is resident, the pipelined variant runs) and the same row inside a
     # batch of 8 (1024 CTAs, more than 4 per SM: the streaming variant runs) share the split plan (8 CTAs
