@@ -15,7 +15,8 @@ Metric: algorithmic HBM GB/s of the whole decode step (bytes the step must
 move: valid K/V, q, outputs, block-table entries, appended rows, logits and
 tokens) divided by the step time, summed over ranks (each rank a replica with
 its own batch: weak scaling, no collective on the data path).  The line also
-carries the step time, the self-attention kernel's roofline, the sampler time,
+carries the step time, the fused layer kernel's roofline, the standalone
+self-attention call timed on its own (self_attn_standalone), the sampler time,
 an end-to-end figure with host buffers, and the CPU oracle timed on a bounded
 sample (cpu_baseline).  --impl reference times that oracle alone.
 """
@@ -792,7 +793,7 @@ def main():
 
     head = measure(w, args.steps, args.warmup, dev, rank, ws, dist, fused=not args.unfused, fp8=fp8,
                    copies=copies, eager=args.eager, decoder_ends=True, e2e=not args.no_e2e,
-                   long_output=True, gpu_index=local)
+                   long_output=True, standalone_self=True, gpu_index=local)
 
     if args.sub == "auto":
         subs = list(SUB_WORKLOADS) if args.workload == 5 and args.layers == 0 and not args.unfused else []
@@ -835,6 +836,8 @@ def main():
         line["kernel_timing"] = ("dominant kernel and sampler: K x layers (K) launches of the timed steps, back to "
                                  "back in their own graph, events around it")
         line["clocks"] = head["clocks"]
+        if "self_attn_standalone" in head:
+            line["self_attn_standalone"] = head["self_attn_standalone"]
         if "long_output" in head:
             line["long_output"] = head["long_output"]
         if sub:
